@@ -1,0 +1,99 @@
+"""The pins catch plausible mistakes: each case plants one mistake in a copy of the
+oracle's source (CPU only, in memory) and checks that a pin check then fails."""
+import math
+import types
+from pathlib import Path
+
+import numpy as np
+import pytest
+import scipy.special
+
+from tests.golden.fixtures import load
+
+SRC = (Path(__file__).resolve().parent.parent / "oracle" / "attention.py").read_text()
+
+
+def _mutant(old: str, new: str):
+    assert SRC.count(old) >= 1, old
+    mod = types.ModuleType("oracle_mutant")
+    exec(compile(SRC.replace(old, new, 1), "oracle_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+def _pins_pass(o) -> bool:
+    """A compact run of the forward, backward and decode pins against module ``o``."""
+    try:
+        rng = np.random.default_rng(3)
+        g = load("anchor_n3_d2.txt")
+        e = math.e
+        out, lse = o.attention_dense(g["Q"], g["K"], g["V"], scale=1.0)
+        np.testing.assert_allclose(out[0], [(e + e * e) / (1 + e + e * e), (1 + e * e) / (1 + e + e * e)], atol=1e-12)
+        np.testing.assert_allclose(lse[0], math.log(1 + e + e * e), atol=1e-12)
+        out, lse = o.attention_dense(g["Q"], g["K"], g["V"], scale=1.0, causal=True)
+        np.testing.assert_allclose(out[:2], [[1, 0], [0.5, 0.5]], atol=1e-12)
+        q, k, v, do = (rng.normal(size=(6, 4)) for _ in range(4))
+        s = np.einsum("id,jd->ij", q, k) / 2.0
+        ref_o = scipy.special.softmax(s, axis=1) @ v
+        out, lse = o.attention_dense(q, k, v)
+        np.testing.assert_allclose(out, ref_o, atol=1e-12)
+        for causal in (False, True):
+            d_o, d_l = o.attention_dense(q, k, v, causal=causal)
+            for block in (1, 2, 4):
+                t_o, t_l = o.attention_tiled_rowwise(q, k, v, block, causal=causal)
+                np.testing.assert_allclose(t_o, d_o, atol=1e-12)
+                np.testing.assert_allclose(t_l, d_l, atol=1e-12)
+            h = 1e-5
+            fd = []
+            for arr in (q, k, v):
+                gr = np.zeros_like(arr)
+                for idx in np.ndindex(arr.shape):
+                    old = arr[idx]
+                    arr[idx] = old + h
+                    plus = np.sum(o.attention_dense(q, k, v, causal=causal)[0] * do)
+                    arr[idx] = old - h
+                    minus = np.sum(o.attention_dense(q, k, v, causal=causal)[0] * do)
+                    arr[idx] = old
+                    gr[idx] = (plus - minus) / (2 * h)
+                fd.append(gr)
+            for a, b in zip(o.attention_dense_backward(q, k, v, do, causal=causal), fd):
+                np.testing.assert_allclose(a, b, atol=2e-8, rtol=2e-6)
+            t_o, t_l = o.attention_tiled_rowwise(q, k, v, 2, causal=causal)
+            for a, b in zip(o.attention_tiled_rowwise_backward(q, k, v, t_o, t_l, do, 2, causal=causal), fd):
+                np.testing.assert_allclose(a, b, atol=2e-8, rtol=2e-6)
+        assert o.split_bounds(10, 4) == [0, 2, 5, 8, 10]
+        qd, kd, vd = rng.normal(size=(1, 8)), rng.normal(size=(13, 8)), rng.normal(size=(13, 8))
+        ref_o, ref_l = o.attention_dense(qd, kd, vd)
+        for n_split in (1, 3, 20):
+            dec_o, dec_l, _ = o.attention_split_decode(qd, kd, vd, n_split)
+            np.testing.assert_allclose(dec_o, ref_o, atol=1e-12)
+            np.testing.assert_allclose(dec_l, ref_l, atol=1e-12)
+    except (AssertionError, ValueError, FloatingPointError):
+        return False
+    return True
+
+
+def test_unmodified_oracle_passes():
+    assert _pins_pass(_mutant("NEG_INF = -np.inf", "NEG_INF = -np.inf"))
+
+
+MUTATIONS = [
+    ("dropped scale", "s = (q_rows @ k.T) * sc", "s = (q_rows @ k.T)"),
+    ("causal off by one", "return kpos > qpos", "return kpos > qpos + 1"),
+    ("lse without max", "lse = m[:, 0] + np.log(", "lse = 0 * m[:, 0] + np.log("),
+    ("no accumulator rescale", "acc = alpha * acc + e @ v[start:stop]", "acc = acc + e @ v[start:stop]"),
+    ("no denominator rescale", "l = alpha * l + e.sum()", "l = l + e.sum()"),
+    ("transposed value rows", "out[h][r0:r1] = p @ v[h]", "out[h][r0:r1] = p @ v[h][::-1]"),
+    ("dropped D term", "ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))", "ds = p * dp"),
+    ("dK from dS not dS^T", "dk[h] += (ds.T @ q_rows) * sc", "dk[h] += (ds @ q_rows) * sc"),
+    ("wrong sign of D (tiled)", "ds = p * (dp - row_dot[i])", "ds = p * (dp + row_dot[i])"),
+    ("dV scaled", "dv[start:stop] += np.outer(p, do[i])", "dv[start:stop] += np.outer(p, do[i]) * sc"),
+    ("merge uses wrong rebase", "a.l * ca + b.l * cb", "a.l * ca + b.l * ca"),
+    ("floor split bounds", "round(Fraction(nk * s, n_split))", "int(Fraction(nk * s, n_split))"),
+    ("decode drops last segment", "for part in parts[1:]:", "for part in parts[1:-1]:"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(name, old, new):
+    with np.errstate(all="ignore"):
+        assert not _pins_pass(_mutant(old, new)), name
