@@ -1,0 +1,479 @@
+#!/usr/bin/env python
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = the whole path once: causal forward and backward on the
+B=2, H=16, N=8192, d=128 workload (Q and K x8, seed 2) and split-KV decode on
+the B=16, H=32, L=32768, d=128, 64-split workload (seed 4).  The headline value
+is forward+backward TFLOP/s (FLOPs 4*B*H*N^2*d, halved when causal, x2.5 for
+the backward); decode is reported as HBM GB/s in its own sub-object.
+
+Prints one JSON line (rank 0).  `--impl reference` times the float64 CPU
+oracle instead (bounded sample of the same workload, host cores).
+Under torchrun each rank runs an independent replica (the path needs no
+exchange between GPUs); the reported time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+_NCORES = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(_NCORES))
+os.environ.setdefault("OMP_NUM_THREADS", str(_NCORES))
+
+import torch  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s & % of bf16 TC peak; decode HBM GB/s"
+FWD_BWD = "causal_fwdbwd_b2h16_n8192_d128_qk8"
+DECODE = "decode_b16h32_l32768_d128_s64"
+
+
+def attention_flops(B, H, N, d, causal, backward):
+    """Matmul FLOPs of attention: 4*N^2*d per head forward, 2.5x that backward
+    (recompute included), halved when causal; softmax exps not counted."""
+    f = 4.0 * B * H * N * N * d
+    if backward:
+        f *= 2.5
+    return f / 2 if causal else f
+
+
+def decode_bytes(B, H, L, d, n_split):
+    """Algorithmic HBM bytes of one decode: K and V read once (bf16), q read,
+    O (fp32) and LSE written, segment states written and read back."""
+    kv = 2 * B * H * L * d * 2
+    q = B * H * d * 2
+    out = B * H * d * 4 + B * H * 4
+    states = 2 * B * H * n_split * (d + 2) * 4
+    return kv + q + out + states
+
+
+def load_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        j = json.loads(p.read_text())
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def source_sha(name):
+    return hashlib.sha256((ROOT / "exact_attention_flash_gb300" / "csrc" / name).read_bytes()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel_file, key):
+    """DRAM bytes per launch recorded from an ncu capture, if the kernel source is unchanged since."""
+    p = ROOT / "profiles" / "traffic.json"
+    if not p.exists():
+        return None
+    rec = json.loads(p.read_text()).get(key)
+    if not rec or rec.get("source_sha") != source_sha(kernel_file):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() and args.impl != "reference" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(w_fb, w_dec, n_heads_fb, n_heads_dec):
+    """Run the float64 oracle on `n_heads` heads of each workload; return
+    (seconds, algorithmic fwd+bwd FLOPs of the sample, decode bytes of the sample)."""
+    import numpy as np
+
+    from exact_attention_flash_gb300.workloads import make_attention_inputs, make_decode_inputs
+    from oracle import attention_dense, attention_dense_backward, attention_split_decode
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    q, k, v, do = make_attention_inputs(1, n_heads_fb, w_fb.N, w_fb.d, w_fb.seed, dev, qk_mult=w_fb.qk_mult)
+    q, k, v, do = (t.double().cpu().numpy() for t in (q, k, v, do))
+    qd, kd, vd = make_decode_inputs(1, n_heads_dec, w_dec.N, w_dec.d, w_dec.seed, dev)
+    qd, kd, vd = (t.double().cpu().numpy() for t in (qd, kd, vd))
+    t0 = time.perf_counter()
+    attention_dense(q, k, v, causal=True)
+    attention_dense_backward(q, k, v, do, causal=True)
+    t1 = time.perf_counter()
+    attention_split_decode(qd, kd, vd, w_dec.n_split)
+    t2 = time.perf_counter()
+    flops = attention_flops(1, n_heads_fb, w_fb.N, w_fb.d, True, False) + attention_flops(
+        1, n_heads_fb, w_fb.N, w_fb.d, True, True)
+    dbytes = decode_bytes(1, n_heads_dec, w_dec.N, w_dec.d, w_dec.n_split)
+    del np
+    return t1 - t0, t2 - t1, flops, dbytes
+
+
+def cpu_baseline_record(heads_fb=1, heads_dec=8):
+    from exact_attention_flash_gb300.workloads import WORKLOADS
+
+    w_fb, w_dec = WORKLOADS[FWD_BWD], WORKLOADS[DECODE]
+    t_fb, t_dec, flops, dbytes = oracle_sample(w_fb, w_dec, heads_fb, heads_dec)
+    return {
+        "value": flops / t_fb / 1e12,
+        "unit": "TFLOP/s",
+        "cores": _NCORES,
+        "kind": "oracle",
+        "sample": f"{heads_fb} of {w_fb.B * w_fb.H} heads of {FWD_BWD} (forward+backward, float64 numpy, "
+                  f"{t_fb:.2f} s); decode: {heads_dec} of {w_dec.B * w_dec.H} heads of {DECODE} ({t_dec:.2f} s, "
+                  f"{dbytes / t_dec / 1e9:.3f} GB/s)",
+        "seconds": t_fb + t_dec,
+        "decode_gbs": dbytes / t_dec / 1e9,
+    }
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    from exact_attention_flash_gb300.workloads import WORKLOADS
+
+    w_fb = WORKLOADS[FWD_BWD]
+    for _ in range(args.warmup):
+        cpu_baseline_record(heads_fb=1, heads_dec=4)
+    vals, secs = [], []
+    rec = None
+    for _ in range(args.steps):
+        rec = cpu_baseline_record(heads_fb=1, heads_dec=4)
+        vals.append(rec["value"])
+        secs.append(rec["seconds"])
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": 1000 * statistics.median(secs),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), bf16-rounded, widened to float64)",
+        "config": {"workload": FWD_BWD, "B": w_fb.B, "H": w_fb.H, "N": w_fb.N, "d": w_fb.d, "causal": True,
+                   "decode_workload": DECODE, "sample": rec["sample"]},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": rec["cores"], "kind": "oracle",
+                         "sample": rec["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU path
+def run_ours(args, world, rank, local):
+    from exact_attention_flash_gb300 import (_lib, backward_workspace_bytes, decode_workspace_bytes, fa_backward,
+                                             fa_decode, fa_device_status, fa_forward)
+    from exact_attention_flash_gb300.build import build
+    from exact_attention_flash_gb300.workloads import WORKLOADS, make_inputs
+
+    if rank == 0 or world > 1:
+        build()
+    barrier(world)
+    _lib.load()
+    dev = torch.device("cuda", local)
+    w, wd = WORKLOADS[FWD_BWD], WORKLOADS[DECODE]
+    q, k, v, do = make_inputs(w, dev)
+    qd, kd, vd = make_inputs(wd, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
+    dq = torch.empty(q.shape, device=dev, dtype=torch.float32)
+    dk = torch.empty_like(dq)
+    dv = torch.empty_like(dq)
+    ws_b = torch.empty(backward_workspace_bytes(w.B, w.H, w.N, w.d), device=dev, dtype=torch.uint8)
+    od = torch.empty((wd.B, wd.H, 1, wd.d), device=dev, dtype=torch.float32)
+    lsed = torch.empty((wd.B, wd.H), device=dev, dtype=torch.float32)
+    ws_d = torch.empty(decode_workspace_bytes(wd.B, wd.H, wd.d, wd.n_split), device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        fa_forward(q, k, v, causal=True, out=o, lse=lse, stream=stream)
+
+    def bwd():
+        fa_backward(q, k, v, o, lse, do, causal=True, workspace=ws_b, dq=dq, dk=dk, dv=dv, stream=stream)
+
+    def dec():
+        fa_decode(qd, kd, vd, wd.n_split, workspace=ws_d, out=od, lse=lsed, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        fwd()
+        bwd()
+        dec()
+    torch.cuda.synchronize(dev)
+    if fa_device_status() != 0:
+        raise RuntimeError("device status not clean after warm-up")
+
+    n = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    for i in range(n):
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        bwd()
+        ev[i][2].record(stream)
+        dec()
+        ev[i][3].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    if fa_device_status() != 0:
+        raise RuntimeError("device status not clean after the timed steps")
+    t_fwd = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)]
+    t_bwd = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]
+    t_dec = [ev[i][2].elapsed_time(ev[i][3]) for i in range(n)]
+    t_step = [ev[i][0].elapsed_time(ev[i][3]) for i in range(n)]
+    fwd_ms = max_over_ranks(sum(t_fwd) / n, world)
+    bwd_ms = max_over_ranks(sum(t_bwd) / n, world)
+    dec_ms = max_over_ranks(sum(t_dec) / n, world)
+    step_ms = max_over_ranks(sum(t_step) / n, world)
+
+    f_fwd = attention_flops(w.B, w.H, w.N, w.d, True, False)
+    f_bwd = attention_flops(w.B, w.H, w.N, w.d, True, True)
+    dbytes = decode_bytes(wd.B, wd.H, wd.N, wd.d, wd.n_split)
+    value = world * (f_fwd + f_bwd) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12
+    peaks = load_peaks()
+
+    # ---- end to end through the public API with host buffers (pinned), copies timed
+    host_in = [t.cpu().pin_memory() for t in (q, k, v, do)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, dq, dk, dv)]
+    dev_in = [torch.empty_like(t) for t in (q, k, v, do)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def e2e_step():
+        for dst, src in zip(dev_in, host_in):
+            dst.copy_(src, non_blocking=True)
+        o2, l2 = fa_forward(dev_in[0], dev_in[1], dev_in[2], causal=True, stream=stream)
+        g = fa_backward(dev_in[0], dev_in[1], dev_in[2], o2, l2, dev_in[3], causal=True, workspace=ws_b,
+                        stream=stream)
+        for dst, src in zip(host_out, (o2, l2) + tuple(g)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n, world)
+    e2e_value = world * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        return
+    bwd_tflops = f_bwd / (bwd_ms * 1e-3) / 1e12
+    fwd_tflops = f_fwd / (fwd_ms * 1e-3) / 1e12
+    dec_gbs = dbytes / (dec_ms * 1e-3) / 1e9
+    cpu = cpu_baseline_record(heads_fb=1, heads_dec=8) if (world == 1 and not args.no_cpu_baseline) else None
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": n,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), bf16; Q,K x8)",
+        "config": {"workload": FWD_BWD, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": True,
+                   "decode_workload": DECODE, "l2": "inputs larger than L2 (K/V stream of 8.6 GB per step)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "kernel": "fa_backward (preprocess + bwd_kernel)", "achieved": bwd_tflops,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": bwd_tflops / peaks["bf16_tflops"],
+                     "traffic": recorded_traffic("fa_bwd.cu", "bwd_kernel_d128_causal"),
+                     "peak_source": peaks["source"] + " burst"},
+        "kernels": {
+            "forward": {"ms": fwd_ms, "tflops": fwd_tflops, "frac_of_bf16_peak": fwd_tflops / peaks["bf16_tflops"],
+                        "traffic": recorded_traffic("fa_fwd.cu", "fwd_kernel_d128_causal")},
+            "backward": {"ms": bwd_ms, "tflops": bwd_tflops, "frac_of_bf16_peak": bwd_tflops / peaks["bf16_tflops"]},
+            "decode": {"ms": dec_ms, "gbs": dec_gbs, "bound": "hbm", "peak_gbs": peaks["hbm_gbs"],
+                       "frac_of_hbm_peak": dec_gbs / peaks["hbm_gbs"], "frac_of_8tbs": dec_gbs / 8000.0,
+                       "algorithmic_bytes": dbytes,
+                       "traffic": recorded_traffic("fa_decode.cu", "decode_split_kernel_d128")},
+        },
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * n,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# Reduced cases for profiler captures: inputs larger than the 129 MB L2, a few GB on the device.
+PROFILE_CASES = {
+    "fwd": dict(B=2, H=32, N=4096, d=128, causal=True, qk_mult=8.0, seed=2),
+    "fwd_d64": dict(B=4, H=32, N=2048, d=64, causal=True, qk_mult=1.0, seed=1),
+    "bwd": dict(B=2, H=32, N=4096, d=128, causal=True, qk_mult=8.0, seed=2),
+    "bwd_d64": dict(B=4, H=32, N=2048, d=64, causal=True, qk_mult=1.0, seed=1),
+    "decode": dict(B=4, H=32, L=32768, d=128, n_split=64, seed=4),
+}
+
+
+def run_profile_case(name, reps):
+    """Launch one kernel family `reps` times on a reduced case (for ncu; prints timing only)."""
+    from exact_attention_flash_gb300 import fa_backward, fa_decode, fa_device_status, fa_forward
+    from exact_attention_flash_gb300.build import build
+    from exact_attention_flash_gb300.workloads import make_attention_inputs, make_decode_inputs
+
+    build()
+    c = PROFILE_CASES[name]
+    if name == "decode":
+        qd, kd, vd = make_decode_inputs(c["B"], c["H"], c["L"], c["d"], c["seed"], "cuda")
+        fn = lambda: fa_decode(qd, kd, vd, c["n_split"])  # noqa: E731
+    else:
+        q, k, v, do = make_attention_inputs(c["B"], c["H"], c["N"], c["d"], c["seed"], "cuda", qk_mult=c["qk_mult"])
+        o, lse = fa_forward(q, k, v, causal=c["causal"])
+        if name.startswith("fwd"):
+            fn = lambda: fa_forward(q, k, v, causal=c["causal"], out=o, lse=lse)  # noqa: E731
+        else:
+            from exact_attention_flash_gb300 import backward_workspace_bytes
+
+            ws = torch.empty(backward_workspace_bytes(c["B"], c["H"], c["N"], c["d"]), device="cuda", dtype=torch.uint8)
+            fn = lambda: fa_backward(q, k, v, o, lse, do, causal=c["causal"], workspace=ws)  # noqa: E731
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    if fa_device_status() != 0:
+        raise RuntimeError("device status not clean")
+    print(json.dumps({"profile_case": name, **c, "reps": reps, "ms_per_call": e0.elapsed_time(e1) / reps}))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--profile", choices=sorted(PROFILE_CASES), help="run one kernel on a reduced case (for ncu)")
+    ap.add_argument("--reps", type=int, default=3)
+    args = ap.parse_args()
+    if args.profile:
+        run_profile_case(args.profile, args.reps)
+        return
+    world, rank, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,117 @@
+"""GB300-native exact tiled attention: forward, recompute backward, split-KV decode.
+
+The Python layer only marshals arguments: torch allocates device memory and
+supplies the stream, and every step of the computation runs in the sm_103a
+kernels of ``libfa_gb300.so`` reached through its C ABI (``include/fa_gb300.h``).
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+from ._lib import FAError
+
+__all__ = ["fa_forward", "fa_backward", "fa_decode", "fa_device_status", "FAError", "backward_workspace_bytes",
+           "decode_workspace_bytes"]
+
+
+def _stream_ptr(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check_bf16(name, t, shape=None):
+    if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _scale_arg(scale):
+    return 0.0 if scale is None else float(scale)
+
+
+def fa_forward(q, k, v, causal=False, scale=None, out_dtype=torch.bfloat16, precise=False, out=None, lse=None,
+               stream=None):
+    """O, LSE = softmax(Q K^T * scale [causal]) V for [B, H, N, d] bf16 inputs."""
+    lib = _lib.load()
+    _check_bf16("q", q)
+    B, H, N, d = q.shape
+    _check_bf16("k", k, q.shape)
+    _check_bf16("v", v, q.shape)
+    if out is None:
+        out = torch.empty((B, H, N, d), device=q.device, dtype=out_dtype)
+    if lse is None:
+        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    o_code = _lib.FA_F32 if out.dtype == torch.float32 else _lib.FA_BF16
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("out dtype must be bf16 or fp32")
+    code = lib.fa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), o_code, lse.data_ptr(),
+                          B, H, N, d, _scale_arg(scale), int(bool(causal)), int(bool(precise)), _stream_ptr(stream))
+    _lib.check("fa_forward", code)
+    return out, lse
+
+
+def backward_workspace_bytes(B, H, N, d) -> int:
+    return int(_lib.load().fa_backward_workspace_size(B, H, N, d))
+
+
+def fa_backward(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, dk=None, dv=None,
+                stream=None):
+    """dQ, dK, dV (fp32) of sum(O * dO) by recomputation from LSE."""
+    lib = _lib.load()
+    _check_bf16("q", q)
+    B, H, N, d = q.shape
+    for name, t in (("k", k), ("v", v), ("do", do)):
+        _check_bf16(name, t, q.shape)
+    if o.dtype not in (torch.bfloat16, torch.float32) or not o.is_contiguous() or tuple(o.shape) != tuple(q.shape):
+        raise ValueError("o must be a contiguous bf16/fp32 tensor shaped like q")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be fp32 [B, H, N]")
+    nbytes = backward_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(nbytes, device=q.device, dtype=torch.uint8)
+    dq = torch.empty(q.shape, device=q.device, dtype=torch.float32) if dq is None else dq
+    dk = torch.empty(q.shape, device=q.device, dtype=torch.float32) if dk is None else dk
+    dv = torch.empty(q.shape, device=q.device, dtype=torch.float32) if dv is None else dv
+    o_code = _lib.FA_F32 if o.dtype == torch.float32 else _lib.FA_BF16
+    code = lib.fa_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), o_code, lse.data_ptr(),
+                           do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                           _scale_arg(scale), int(bool(causal)), workspace.data_ptr(), workspace.numel(),
+                           _stream_ptr(stream))
+    _lib.check("fa_backward", code)
+    return dq, dk, dv
+
+
+def decode_workspace_bytes(B, H, d, n_split) -> int:
+    return int(_lib.load().fa_decode_workspace_size(B, H, d, n_split))
+
+
+def fa_decode(q, k, v, n_split, scale=None, return_partials=False, workspace=None, out=None, lse=None,
+              stream=None):
+    """Split-KV decode: q [B, H, 1, d], k/v [B, H, L, d] bf16 -> O [B, H, 1, d] fp32, LSE [B, H]."""
+    lib = _lib.load()
+    _check_bf16("q", q)
+    _check_bf16("k", k)
+    _check_bf16("v", v, k.shape)
+    B, H, L, d = k.shape
+    if tuple(q.shape) != (B, H, 1, d):
+        raise ValueError("q must be [B, H, 1, d]")
+    if workspace is None:
+        workspace = torch.empty(decode_workspace_bytes(B, H, d, max(int(n_split), 1)), device=q.device,
+                                dtype=torch.uint8)
+    out = torch.empty((B, H, 1, d), device=q.device, dtype=torch.float32) if out is None else out
+    lse = torch.empty((B, H), device=q.device, dtype=torch.float32) if lse is None else lse
+    parts = None
+    if return_partials:
+        parts = torch.empty((B, H, max(int(n_split), 1), d + 2), device=q.device, dtype=torch.float32)
+    code = lib.fa_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, L, d,
+                         _scale_arg(scale), int(n_split), 0 if parts is None else parts.data_ptr(),
+                         workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
+    _lib.check("fa_decode", code)
+    return (out, lse, parts) if return_partials else (out, lse)
+
+
+def fa_device_status(stream=None) -> int:
+    """Synchronise and return (and clear) the kernels' device status as an fa_status code."""
+    return int(_lib.load().fa_device_status(_stream_ptr(stream)))

@@ -1,0 +1,205 @@
+// C ABI: argument checks, TMA descriptor set-up and launches on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fa_gb300.h"
+#include "internal.h"
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// [B*H, N, d] bf16 viewed as a 3-D tensor (d innermost), tiles of `box_rows` rows x
+// 64 features (128 bytes, the swizzle width); rows past N read as zero.
+fa_status make_row_tile_map(CUtensorMap* m, const void* ptr, int BH, int N, int d, int box_rows = 128) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return FA_ERR_CUDA;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, elem,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status check_common(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H > 65535LL) return FA_ERR_UNSUPPORTED;  // grid.x holds B*H for fwd/bwd
+  return FA_OK;
+}
+
+float resolve_scale(float scale, int d) { return scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(d)); }
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+extern "C" {
+
+int fa_abi_version(void) { return FA_ABI_VERSION; }
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "device wait timed out";
+    case FA_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+fa_status fa_forward(const void* q, const void* k, const void* v, void* o, fa_dtype o_dtype, float* lse, int B,
+                     int H, int N, int d, float scale, int causal, int precise, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  if (o_dtype != FA_BF16 && o_dtype != FA_F32) return FA_ERR_INVALID_ARG;
+  fa_status st = check_common(B, H, N, d);
+  if (st != FA_OK) return st;
+  fa::ForwardArgs a{};
+  const int BH = B * H;
+  if ((st = make_row_tile_map(&a.tm_q, q, BH, N, d)) != FA_OK) return st;
+  if ((st = make_row_tile_map(&a.tm_k, k, BH, N, d)) != FA_OK) return st;
+  if ((st = make_row_tile_map(&a.tm_v, v, BH, N, d)) != FA_OK) return st;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.d = d;
+  a.scale_log2 = resolve_scale(scale, d) * kLog2e;
+  a.causal = causal ? 1 : 0;
+  a.o_f32 = (o_dtype == FA_F32) ? 1 : 0;
+  a.precise = precise ? 1 : 0;
+  return fa::launch_forward(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_backward_workspace_size(int B, int H, int N, int d) {
+  (void)d;
+  if (B < 1 || H < 1 || N < 1) return 0;
+  return round_up(static_cast<size_t>(B) * H * N * sizeof(float), 256);
+}
+
+fa_status fa_backward(const void* q, const void* k, const void* v, const void* o, fa_dtype o_dtype,
+                      const float* lse, const void* dout, float* dq, float* dk, float* dv, int B, int H, int N, int d,
+                      float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_INVALID_ARG;
+  if (o_dtype != FA_BF16 && o_dtype != FA_F32) return FA_ERR_INVALID_ARG;
+  fa_status st = check_common(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < fa_backward_workspace_size(B, H, N, d))
+    return FA_ERR_WORKSPACE;
+  fa::BackwardArgs a{};
+  const int BH = B * H;
+  if ((st = make_row_tile_map(&a.tm_q, q, BH, N, d, 64)) != FA_OK) return st;
+  if ((st = make_row_tile_map(&a.tm_k, k, BH, N, d, 128)) != FA_OK) return st;
+  if ((st = make_row_tile_map(&a.tm_v, v, BH, N, d, 128)) != FA_OK) return st;
+  if ((st = make_row_tile_map(&a.tm_do, dout, BH, N, d, 64)) != FA_OK) return st;
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.delta = static_cast<float*>(workspace);
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.d = d;
+  a.scale = resolve_scale(scale, d);
+  a.scale_log2 = a.scale * kLog2e;
+  a.causal = causal ? 1 : 0;
+  a.o_f32 = (o_dtype == FA_F32) ? 1 : 0;
+  const cudaError_t e = fa::launch_backward(a, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_decode_workspace_size(int B, int H, int d, int n_split) {
+  if (B < 1 || H < 1 || n_split < 1 || d < 1) return 0;
+  const size_t counters = round_up(static_cast<size_t>(B) * H * sizeof(unsigned), 256);
+  const size_t partials = static_cast<size_t>(B) * H * n_split * (d + 2) * sizeof(float);
+  return counters + round_up(partials, 256);
+}
+
+fa_status fa_decode(const void* q, const void* k, const void* v, float* o, float* lse, int B, int H, int L, int d,
+                    float scale, int n_split, float* partials, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return FA_ERR_INVALID_ARG;
+  if (n_split < 1 || L < 1 || B < 1 || H < 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (B > 65535 || H > 65535 || n_split > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < fa_decode_workspace_size(B, H, d, n_split))
+    return FA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t counter_bytes = round_up(static_cast<size_t>(B) * H * sizeof(unsigned), 256);
+  fa::DecodeArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.partials = partials;
+  a.ws_counters = static_cast<unsigned*>(workspace);
+  a.ws_partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + counter_bytes);
+  a.B = B;
+  a.H = H;
+  a.L = L;
+  a.d = d;
+  a.n_split = n_split;
+  a.scale_log2 = resolve_scale(scale, d) * kLog2e;
+  if (cudaMemsetAsync(a.ws_counters, 0, static_cast<size_t>(B) * H * sizeof(unsigned), s) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return fa::launch_decode(a, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_device_status(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned f = 0, b = 0, dcd = 0;
+  if (fa::read_clear_forward_status(&f, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (fa::read_clear_backward_status(&b, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (fa::read_clear_decode_status(&dcd, s) != cudaSuccess) return FA_ERR_CUDA;
+  const unsigned all = f | b | dcd;
+  if (all & 1u) return FA_ERR_TIMEOUT;
+  if (all != 0u) return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+fa_status fa_debug_wait_timeout(unsigned long long limit_ns, void* stream) {
+  if (limit_ns == 0 || limit_ns > 5000000000ull) return FA_ERR_INVALID_ARG;
+  return fa::launch_wait_timeout_probe(limit_ns, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
+                                                                                                   : FA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,401 @@
+// Exact attention backward on sm_103a: P is recomputed from the stored
+// log-sum-exp, nothing of size N x N is stored.
+//
+// What it computes ("attention_kernels.py", CMU 15-779 lecture 5, section 4
+// ``flash_backward``; "lab.py" ``backward``): D = rowsum(dO * O); for each key
+// tile j and query tile i, S = Q_i K_j^T * scale, P = exp(S - L_i),
+// dV_j += P^T dO_i, dP = dO_i V_j^T, dS = P * (dP - D_i),
+// dQ_i += dS K_j * scale, dK_j += dS^T Q_i * scale.  Causal: query tiles that
+// lie wholly before the key tile are skipped; the others are masked per element.
+//
+// Kernels:
+//   bwd_preprocess  one warp per row: D = rowsum(dO * O), and dQ := 0.
+//   bwd_kernel      one CTA per (128-key tile, batch*head); it walks the query
+//                   tiles of 64 rows.  Keys are the TMEM lanes, so the kernel
+//                   forms the transposed products:
+//       S^T = K Q_i^T and dP^T = V dO_i^T        (SS MMA, M=128, N=64)
+//       dV += P^T dO_i and dK += dS^T Q_i        (TS MMA, A = P^T / dS^T in TMEM)
+//       dQ_i^T = K^T dS_i^T                      (SS MMA, M=d, N=64, dS from smem)
+//   warp 8 loads (TMA), warp 9 issues MMAs, warps 0-3 (thread = key) turn S^T,
+//   dP^T into P^T, dS^T, warps 4-7 (thread = feature) add dQ_i^T into dQ with
+//   fp32 reductions in L2.  S^T/dP^T are double-buffered in TMEM so the tensor
+//   core computes step n+1 while step n's elementwise work runs; dQ^T of step
+//   n lands in the S^T buffer that P^T of step n has just left.
+// Tensor memory (512 columns): S^T[2] [0,64) [64,128), dP^T[2] [128,192)
+// [192,256), dV [256, 256+d), dK [256+d, 256+2d).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+__device__ unsigned g_bwd_status;
+
+constexpr int kBKV = 128;  // keys per CTA
+constexpr int kBQ = 64;    // queries per step
+constexpr int kBwdThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kKVBytes = kBKV * D * 2;   // K or V tile
+  static constexpr int kQBytes = kBQ * D * 2;     // Q or dO tile
+  static constexpr int kStages = (D == 128) ? 3 : 4;
+  static constexpr int kDSBytes = kBKV * kBQ * 2; // dS tile (bf16), 16 KB
+  static constexpr int kDVCol = 256;
+  static constexpr int kDKCol = 256 + D;
+  static constexpr int kSmemBytes = 2 * kKVBytes + kStages * 2 * kQBytes + 2 * kDSBytes + 1024;
+};
+
+struct BwdShared {
+  uint64_t kv_full;
+  uint64_t q_full[4], q_empty[4];
+  uint64_t sdp_full[2], p_full[2], dq_full[2], dq_empty[2], ds_empty[2];
+  uint64_t dkdv_full;
+  uint64_t drain;
+  float lse2[2][kBQ];
+  float delta[2][kBQ];
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void compute_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_constant__ BackwardArgs a) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = sK + C::kKVBytes;
+  uint8_t* sQ = sV + C::kKVBytes;                       // [kStages][kQBytes]
+  uint8_t* sDO = sQ + C::kStages * C::kQBytes;          // [kStages][kQBytes]
+  uint8_t* sDS = sDO + C::kStages * C::kQBytes;         // [2][kDSBytes]
+  __shared__ BwdShared sh;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x;
+  const int j = blockIdx.y;           // key tile; small j carries the most causal work, so it starts first
+  const int key0 = j * kBKV;
+  const int n_q = (a.N + kBQ - 1) / kBQ;
+  const int i_start = a.causal ? key0 / kBQ : 0;
+  const int n_steps = n_q - i_start;
+
+  if (tid == 0) {
+    sh.abort = 0;
+    mbar_init(&sh.kv_full, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&sh.q_full[s], 1);
+      mbar_init(&sh.q_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sh.sdp_full[b], 1);
+      mbar_init(&sh.p_full[b], 128);
+      mbar_init(&sh.dq_full[b], 1);
+      mbar_init(&sh.dq_empty[b], 128);
+      mbar_init(&sh.ds_empty[b], 1);
+    }
+    mbar_init(&sh.dkdv_full, 1);
+    mbar_init(&sh.drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) tmem_alloc(&sh.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&a.tm_q);
+      tma_prefetch_desc(&a.tm_k);
+      tma_prefetch_desc(&a.tm_v);
+      tma_prefetch_desc(&a.tm_do);
+      mbar_arrive_expect_tx(&sh.kv_full, 2 * C::kKVBytes);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(sK + c * (kBKV * 128), &a.tm_k, &sh.kv_full, c * 64, key0, bh);
+        tma_load_3d(sV + c * (kBKV * 128), &a.tm_v, &sh.kv_full, c * 64, key0, bh);
+      }
+      int issued = 0;
+      for (int n = 0; n < n_steps; ++n) {
+        const int s = n % C::kStages;
+        if (n >= C::kStages && !mbar_wait(&sh.q_empty[s], ((n / C::kStages) - 1) & 1, &sh.abort, &g_bwd_status))
+          break;
+        const int q0 = (i_start + n) * kBQ;
+        mbar_arrive_expect_tx(&sh.q_full[s], 2 * C::kQBytes);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d(sQ + s * C::kQBytes + c * (kBQ * 128), &a.tm_q, &sh.q_full[s], c * 64, q0, bh);
+          tma_load_3d(sDO + s * C::kQBytes + c * (kBQ * 128), &a.tm_do, &sh.q_full[s], c * 64, q0, bh);
+        }
+        ++issued;
+      }
+      mbar_wait_drain(&sh.kv_full, 0);
+      for (int n = max(0, issued - C::kStages); n < issued; ++n)
+        mbar_wait_drain(&sh.q_full[n % C::kStages], (n / C::kStages) & 1);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdSdP = idesc_bf16_f32(kBKV, kBQ, false, false);  // S^T, dP^T
+      constexpr uint32_t kIdKV = idesc_bf16_f32(kBKV, D, false, true);      // dV, dK (A in TMEM)
+      constexpr uint32_t kIdQ = idesc_bf16_f32(128, kBQ, true, true);       // dQ^T = K^T dS^T
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aDO = smem_u32(sDO),
+                     aDS = smem_u32(sDS);
+      bool ok = mbar_wait(&sh.kv_full, 0, &sh.abort, &g_bwd_status);
+      auto issue_sdp = [&](int n) -> bool {
+        const int s = n % C::kStages, b = n & 1;
+        if (!mbar_wait(&sh.q_full[s], (n / C::kStages) & 1, &sh.abort, &g_bwd_status)) return false;
+        if (n >= 2 && !mbar_wait(&sh.dq_empty[b], ((n >> 1) - 1) & 1, &sh.abort, &g_bwd_status)) return false;
+        tc_fence_after();
+        const uint32_t q_a = aQ + s * C::kQBytes, do_a = aDO + s * C::kQBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t kv_off = (kk >> 2) * (kBKV * 128) + (kk & 3) * 32;
+          const uint32_t q_off = (kk >> 2) * (kBQ * 128) + (kk & 3) * 32;
+          umma_ss(tmem_addr(tmem, 0, b * kBQ), sdesc_sw128(aK + kv_off, 16, 1024), sdesc_sw128(q_a + q_off, 16, 1024),
+                  kIdSdP, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t kv_off = (kk >> 2) * (kBKV * 128) + (kk & 3) * 32;
+          const uint32_t q_off = (kk >> 2) * (kBQ * 128) + (kk & 3) * 32;
+          umma_ss(tmem_addr(tmem, 0, 128 + b * kBQ), sdesc_sw128(aV + kv_off, 16, 1024),
+                  sdesc_sw128(do_a + q_off, 16, 1024), kIdSdP, kk > 0);
+        }
+        umma_commit(&sh.sdp_full[b]);
+        return true;
+      };
+      if (ok) {
+        tc_fence_after();
+        ok = issue_sdp(0);
+      }
+      for (int n = 0; ok && n < n_steps; ++n) {
+        const int s = n % C::kStages, b = n & 1;
+        if (n + 1 < n_steps && !issue_sdp(n + 1)) break;
+        if (!mbar_wait(&sh.p_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status)) break;
+        tc_fence_after();
+        const uint32_t q_a = aQ + s * C::kQBytes, do_a = aDO + s * C::kQBytes;
+        // dV += P^T dO_i   (K = 64 queries; dO_i is the MN-major B operand)
+#pragma unroll
+        for (int kk = 0; kk < kBQ / 16; ++kk)
+          umma_ts(tmem_addr(tmem, 0, C::kDVCol), tmem_addr(tmem, 0, b * kBQ + kk * 8),
+                  sdesc_sw128(do_a + kk * 16 * 128, kBQ * 128, 1024), kIdKV, (n > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q_i
+#pragma unroll
+        for (int kk = 0; kk < kBQ / 16; ++kk)
+          umma_ts(tmem_addr(tmem, 0, C::kDKCol), tmem_addr(tmem, 0, 128 + b * kBQ + kk * 8),
+                  sdesc_sw128(q_a + kk * 16 * 128, kBQ * 128, 1024), kIdKV, (n > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&sh.q_empty[s]);
+        // dQ_i^T = K^T dS^T into the S^T buffer (its P^T was consumed by the dV MMA above).
+        // A = K as an MN-major [d x keys] operand; for d = 64 the upper 64 rows of the
+        // M = 128 product read the V tile and are ignored.
+        const uint32_t ds_a = aDS + b * C::kDSBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBKV / 16; ++kk)
+          umma_ss(tmem_addr(tmem, 0, b * kBQ), sdesc_sw128(aK + kk * 16 * 128, kBKV * 128, 1024),
+                  sdesc_sw128(ds_a + kk * 16 * 128, kBKV * 128, 1024), kIdQ, kk > 0);
+        umma_commit(&sh.dq_full[b]);
+        umma_commit(&sh.ds_empty[b]);
+      }
+      if (ok) umma_commit(&sh.dkdv_full);
+      umma_commit(&sh.drain);
+      mbar_wait_drain(&sh.drain, 0);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ P^T and dS^T (thread = key)
+    const int k = tid;
+    const int key = key0 + k;
+    const int lane_base = warp * 32;
+    const float sl2 = a.scale_log2;
+    bool ok = true;
+    for (int n = 0; n < n_steps; ++n) {
+      const int b = n & 1;
+      const int q0 = (i_start + n) * kBQ;
+      {
+        const int qq = q0 + (k & (kBQ - 1));
+        const size_t idx = static_cast<size_t>(bh) * a.N + qq;
+        if (k < kBQ)
+          sh.lse2[b][k] = (qq < a.N) ? a.lse[idx] * kLog2e : INFINITY;
+        else
+          sh.delta[b][k - kBQ] = (qq < a.N) ? a.delta[idx] : 0.f;
+      }
+      compute_bar_sync();
+      if (!__all_sync(0xffffffffu, mbar_wait(&sh.sdp_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status))) {
+        ok = false;
+        break;
+      }
+      if (n >= 2 && !__all_sync(0xffffffffu, mbar_wait(&sh.ds_empty[b], ((n >> 1) - 1) & 1, &sh.abort, &g_bwd_status))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool need_mask = (a.causal && key0 + kBKV - 1 > q0) || (key0 + kBKV > a.N);
+      const int first_visible_q = a.causal ? key : 0;  // queries before this key see nothing of it
+      const bool key_valid = key < a.N;
+      const uint32_t s_tm = tmem_addr(tmem, lane_base, b * kBQ);
+      const uint32_t dp_tm = tmem_addr(tmem, lane_base, 128 + b * kBQ);
+      uint8_t* ds_row = sDS + b * C::kDSBytes + (k >> 3) * 1024 + (k & 7) * 128;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sv[32], dpv[32];
+        tmem_ld32(s_tm + 32 * c, sv);
+        tmem_ld32(dp_tm + 32 * c, dpv);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float p[2], ds[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col = 32 * c + e + u;
+            float pv = ex2(fmaf(__uint_as_float(sv[e + u]), sl2, -sh.lse2[b][col]));
+            if (need_mask && (!key_valid || q0 + col < first_visible_q)) pv = 0.f;
+            p[u] = pv;
+            ds[u] = pv * (__uint_as_float(dpv[e + u]) - sh.delta[b][col]);
+          }
+          pk[e / 2] = pack_bf16(p[0], p[1]);
+          dk[e / 2] = pack_bf16(ds[0], ds[1]);
+        }
+        tmem_st16(s_tm + 16 * c, pk);
+        tmem_st16(dp_tm + 16 * c, dk);
+        // dS^T row of this key into the MN-major, 128B-swizzled dS tile:
+        // 16-byte piece p (queries 8p..8p+7) of row k sits at ((p ^ (k & 7)) * 16).
+#pragma unroll
+        for (int pc = 0; pc < 4; ++pc) {
+          const int piece = 4 * c + pc;
+          *reinterpret_cast<uint4*>(ds_row + ((piece ^ (k & 7)) << 4)) =
+              make_uint4(dk[4 * pc], dk[4 * pc + 1], dk[4 * pc + 2], dk[4 * pc + 3]);
+        }
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      mbar_arrive(&sh.p_full[b]);
+    }
+    // ------------------------------------------------------------ dK, dV epilogue
+    if (ok && __all_sync(0xffffffffu, mbar_wait(&sh.dkdv_full, 0, &sh.abort, &g_bwd_status))) {
+      tc_fence_after();
+      const size_t row_off = (static_cast<size_t>(bh) * a.N + key) * D;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t uv[32], uk[32];
+        tmem_ld32(tmem_addr(tmem, lane_base, C::kDVCol + c), uv);
+        tmem_ld32(tmem_addr(tmem, lane_base, C::kDKCol + c), uk);
+        if (key < a.N) {
+          float4* dv = reinterpret_cast<float4*>(a.dv + row_off + c);
+          float4* dkp = reinterpret_cast<float4*>(a.dk + row_off + c);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            dv[i] = make_float4(__uint_as_float(uv[4 * i]), __uint_as_float(uv[4 * i + 1]),
+                                __uint_as_float(uv[4 * i + 2]), __uint_as_float(uv[4 * i + 3]));
+            dkp[i] = make_float4(__uint_as_float(uk[4 * i]) * a.scale, __uint_as_float(uk[4 * i + 1]) * a.scale,
+                                 __uint_as_float(uk[4 * i + 2]) * a.scale, __uint_as_float(uk[4 * i + 3]) * a.scale);
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ writer (thread = feature)
+    const int c = tid - 128;                 // feature index == TMEM lane of dQ^T
+    const int lane_base = (warp & 3) * 32;
+    const bool has_rows = lane_base < D;     // for d = 64, lanes 64..127 hold no feature
+    for (int n = 0; n < n_steps; ++n) {
+      const int b = n & 1;
+      const int q0 = (i_start + n) * kBQ;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sh.dq_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status))) break;
+      tc_fence_after();
+      uint32_t v[64];
+      if (has_rows) tmem_ld64(tmem_addr(tmem, lane_base, b * kBQ), v);
+      tc_fence_before();
+      mbar_arrive(&sh.dq_empty[b]);
+      if (has_rows) {
+        float* dst = a.dq + (static_cast<size_t>(bh) * a.N + q0) * D + c;
+        const int rows = min(kBQ, a.N - q0);
+#pragma unroll
+        for (int q = 0; q < kBQ; ++q)
+          if (q < rows) atomicAdd(dst + static_cast<size_t>(q) * D, __uint_as_float(v[q]) * a.scale);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// One warp per query row: D = rowsum(dO * O) and dQ := 0 for the row.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_preprocess(const void* __restrict__ o, int o_f32,
+                                                       const __nv_bfloat16* __restrict__ dout,
+                                                       float* __restrict__ delta, float* __restrict__ dq,
+                                                       long long rows) {
+  constexpr int kPer = D / 32;
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const size_t base = static_cast<size_t>(row) * D + lane * kPer;
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const float ov = o_f32 ? static_cast<const float*>(o)[base + i]
+                           : __bfloat162float(static_cast<const __nv_bfloat16*>(o)[base + i]);
+    acc = fmaf(__bfloat162float(dout[base + i]), ov, acc);
+    dq[base + i] = 0.f;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) delta[row] = acc;
+}
+
+template <int D>
+cudaError_t launch_bwd_t(const BackwardArgs& a, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  const long long rows = static_cast<long long>(a.B) * a.H * a.N;
+  bwd_preprocess<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+      a.o, a.o_f32, static_cast<const __nv_bfloat16*>(a.dout), a.delta, a.dq, rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.B * a.H, (a.N + kBKV - 1) / kBKV);
+  bwd_kernel<D><<<grid, kBwdThreads, C::kSmemBytes, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t stream) {
+  if (a.d == 128) return launch_bwd_t<128>(a, stream);
+  if (a.d == 64) return launch_bwd_t<64>(a, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t read_clear_backward_status(unsigned* out, cudaStream_t stream) {
+  cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_bwd_status, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return e;
+  const unsigned zero = 0;
+  e = cudaMemcpyToSymbolAsync(g_bwd_status, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(stream);
+}
+
+}  // namespace fa

@@ -1,0 +1,404 @@
+// Exact attention forward on sm_103a: TMA tile loads, tcgen05 MMAs accumulating
+// in tensor memory, online softmax in registers.
+//
+// What it computes ("attention_kernels.py", CMU 15-779 lecture 5, section 3
+// ``flash_forward``; "lab.py" ``tiled``): for each query row, over key tiles,
+// S = Q K^T * scale, m' = max(m, rowmax S), P = exp(S - m'), l = l * exp(m - m')
+// + rowsum P, acc = acc * exp(m - m') + P V, and at the end O = acc / l and
+// L = m + ln l.  Causal: key j is visible to query i iff j <= i; key tiles
+// wholly in the future of a query tile are skipped, and only the diagonal tile
+// is masked.
+//
+// GPU design (one CTA = two 128-row query tiles, 256 rows):
+//   warp 8      TMA producer: both Q tiles once, then K and V tiles of 128 keys
+//               through a ring of shared-memory stages.
+//   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into TMEM (SS MMA),
+//               O_t += P_t V_j with P read from TMEM (TS MMA), interleaving the
+//               two tiles so the tensor core works on one tile while the other
+//               tile's softmax runs.
+//   warps 0-3   softmax for tile 0, warps 4-7 for tile 1: thread r owns query
+//               row r (TMEM lane r), loads its row of S, takes the row max in
+//               registers, writes P as bf16 over the S columns, and rescales its
+//               row of O in TMEM when the running max grows by more than 2^8
+//               (the final O / l uses the same reference max, so this is exact).
+// Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 and O_1 after.
+// Work is done in base 2: x = S * scale * log2(e), p = 2^(x - m).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+__device__ unsigned g_fwd_status;
+
+constexpr int kBM = 128;             // query rows per tile (TMEM lanes)
+constexpr int kBN = 128;             // keys per KV tile
+constexpr int kTiles = 2;            // query tiles per CTA
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kFwdThreads = 320;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kChunks = D / 64;                // 128-byte swizzle chunks per row
+  static constexpr int kTileBytes = kBM * D * 2;        // one 128-row bf16 tile
+  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kOCol = 256;                     // O_0 column; O_1 at kOCol + D
+  static constexpr int kSmemBytes = kTiles * kTileBytes + kStages * 2 * kTileBytes + 1024;
+};
+
+struct FwdBarriers {
+  uint64_t q_full;
+  uint64_t k_full[4], v_full[4], kv_empty[4];
+  uint64_t s_full[kTiles], p_full[kTiles], o_full[kTiles];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D, bool kPrecise>
+__global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ ForwardArgs a) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;                                   // [kTiles][kTileBytes]
+  uint8_t* sK = smem + kTiles * C::kTileBytes;          // [kStages][kTileBytes]
+  uint8_t* sV = sK + C::kStages * C::kTileBytes;        // [kStages][kTileBytes]
+  __shared__ FwdBarriers bars;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x;
+  const int q_row0 = (gridDim.y - 1 - blockIdx.y) * (kBM * kTiles);  // heaviest query blocks first
+  const int n_kv_total = (a.N + kBN - 1) / kBN;
+  int n_kv[kTiles];
+#pragma unroll
+  for (int t = 0; t < kTiles; ++t)
+    n_kv[t] = a.causal ? min(n_kv_total, (q_row0 + t * kBM) / kBN + 1) : n_kv_total;
+  const int n_kv_cta = n_kv[kTiles - 1];
+
+  if (tid == 0) {
+    bars.abort = 0;
+    mbar_init(&bars.q_full, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars.k_full[s], 1);
+      mbar_init(&bars.v_full[s], 1);
+      mbar_init(&bars.kv_empty[s], 1);
+    }
+    for (int t = 0; t < kTiles; ++t) {
+      mbar_init(&bars.s_full[t], 1);
+      mbar_init(&bars.p_full[t], kBM);
+      mbar_init(&bars.o_full[t], 1);
+    }
+    mbar_init(&bars.drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) tmem_alloc(&bars.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&a.tm_q);
+      tma_prefetch_desc(&a.tm_k);
+      tma_prefetch_desc(&a.tm_v);
+      mbar_arrive_expect_tx(&bars.q_full, kTiles * C::kTileBytes);
+      for (int t = 0; t < kTiles; ++t)
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(sQ + t * C::kTileBytes + c * (kBM * 128), &a.tm_q, &bars.q_full, c * 64, q_row0 + t * kBM, bh);
+      int issued = 0;
+      for (int j = 0; j < n_kv_cta; ++j) {
+        const int s = j % C::kStages;
+        if (j >= C::kStages && !mbar_wait(&bars.kv_empty[s], ((j / C::kStages) - 1) & 1, &bars.abort, &g_fwd_status))
+          break;
+        uint8_t* k_dst = sK + s * C::kTileBytes;
+        uint8_t* v_dst = sV + s * C::kTileBytes;
+        mbar_arrive_expect_tx(&bars.k_full[s], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(k_dst + c * (kBN * 128), &a.tm_k, &bars.k_full[s], c * 64, j * kBN, bh);
+        mbar_arrive_expect_tx(&bars.v_full[s], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(v_dst + c * (kBN * 128), &a.tm_v, &bars.v_full[s], c * 64, j * kBN, bh);
+        ++issued;
+      }
+      // Drain: every copy this CTA started must land before shared memory is released.
+      mbar_wait_drain(&bars.q_full, 0);
+      for (int j = max(0, issued - C::kStages); j < issued; ++j) {
+        const int s = j % C::kStages;
+        mbar_wait_drain(&bars.k_full[s], (j / C::kStages) & 1);
+        mbar_wait_drain(&bars.v_full[s], (j / C::kStages) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, false, false);
+      constexpr uint32_t kIdO = idesc_bf16_f32(kBM, D, false, true);
+      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+      auto issue_s = [&](int t, int j) {
+        const int s = j % C::kStages;
+        const uint32_t qa = sQa + t * C::kTileBytes, ka = sKa + s * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+          umma_ss(tmem_addr(tmem, 0, t * kBN), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                  kIdS, kk > 0);
+        }
+        umma_commit(&bars.s_full[t]);
+      };
+      auto issue_pv = [&](int t, int j) {
+        const int s = j % C::kStages;
+        const uint32_t va = sVa + s * C::kTileBytes;
+        const uint32_t o_tm = tmem_addr(tmem, 0, C::kOCol + t * D);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          umma_ts(o_tm, tmem_addr(tmem, 0, t * kBN + kk * 8), sdesc_sw128(va + kk * 16 * 128, kBN * 128, 1024), kIdO,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+        if (kPrecise) {
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            umma_ts(o_tm, tmem_addr(tmem, 0, t * kBN + 64 + kk * 8), sdesc_sw128(va + kk * 16 * 128, kBN * 128, 1024),
+                    kIdO, 1u);
+        }
+      };
+      bool ok = mbar_wait(&bars.q_full, 0, &bars.abort, &g_fwd_status) &&
+                mbar_wait(&bars.k_full[0], 0, &bars.abort, &g_fwd_status);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < kTiles; ++t) issue_s(t, 0);
+      }
+      for (int j = 0; ok && j < n_kv_cta; ++j) {
+        const int s = j % C::kStages;
+        const int jn = j + 1, sn = jn % C::kStages;
+        if (!mbar_wait(&bars.v_full[s], (j / C::kStages) & 1, &bars.abort, &g_fwd_status)) break;
+        // tile 0
+        if (j < n_kv[0]) {
+          if (!mbar_wait(&bars.p_full[0], j & 1, &bars.abort, &g_fwd_status)) break;
+          tc_fence_after();
+          issue_pv(0, j);
+          if (jn < n_kv[0]) {
+            if (!mbar_wait(&bars.k_full[sn], (jn / C::kStages) & 1, &bars.abort, &g_fwd_status)) break;
+            tc_fence_after();
+            issue_s(0, jn);
+          } else {
+            umma_commit(&bars.o_full[0]);
+          }
+        }
+        // tile 1
+        if (!mbar_wait(&bars.p_full[1], j & 1, &bars.abort, &g_fwd_status)) break;
+        tc_fence_after();
+        issue_pv(1, j);
+        umma_commit(&bars.kv_empty[s]);
+        if (jn < n_kv[1]) {
+          if (!mbar_wait(&bars.k_full[sn], (jn / C::kStages) & 1, &bars.abort, &g_fwd_status)) break;
+          tc_fence_after();
+          issue_s(1, jn);
+        } else {
+          umma_commit(&bars.o_full[1]);
+        }
+      }
+      // Drain: all MMAs complete before tensor memory is released.
+      umma_commit(&bars.drain);
+      mbar_wait_drain(&bars.drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;                  // query tile of this warpgroup
+    const int r = tid - t * kBM;              // row within the tile == TMEM lane
+    const int lane_base = (warp & 3) * 32;    // TMEM lane quarter of this warp
+    const int row = q_row0 + t * kBM + r;
+    const uint32_t s_tm = tmem_addr(tmem, lane_base, t * kBN);
+    const uint32_t o_tm = tmem_addr(tmem, lane_base, C::kOCol + t * D);
+    const float sl2 = a.scale_log2;
+    float m_run = -INFINITY;  // reference max (scaled, log2 units)
+    float l_run = 0.f;  // sum of p: the log-sum-exp
+    float l_hat = 0.f;  // sum of the bf16-rounded p that enter P V: the normaliser of O
+    bool ok = true;
+    for (int j = 0; j < n_kv[t]; ++j) {
+      // Lanes leave together: the TMEM accesses below are warp-collective.
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars.s_full[t], j & 1, &bars.abort, &g_fwd_status))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float x[kBN];
+      {
+        uint32_t u[64];
+        tmem_ld64(s_tm, u);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(u[i]);
+        tmem_ld64(s_tm + 64, u);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) x[64 + i] = __uint_as_float(u[i]);
+      }
+      const int key0 = j * kBN;
+      const bool need_mask = (key0 + kBN > a.N) || (a.causal && key0 + kBN - 1 > q_row0 + t * kBM);
+      if (need_mask) {
+        const int lim = a.causal ? min(a.N - 1, row) : a.N - 1;  // last visible key
+#pragma unroll
+        for (int i = 0; i < kBN; ++i)
+          if (key0 + i > lim) x[i] = -INFINITY;
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int i = 1; i < kBN; ++i) mx = fmaxf(mx, x[i]);
+      const float m_tile = mx * sl2;
+      float m_use = m_run;
+      float alpha = 1.f;
+      if (m_tile > m_run + kRescaleThreshold) {
+        m_use = m_tile;
+        alpha = ex2(m_run - m_use);  // 0 on the first tile
+      }
+      // Rescale this row of O when the reference max moved (not on the first
+      // tile: O is written, not accumulated, by the first PV).
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        for (int c = 0; c < D; c += 32) {
+          uint32_t u[32];
+          tmem_ld32(o_tm + c, u);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+          tmem_st32(o_tm + c, u);
+        }
+      }
+      const float neg_m = (m_use == -INFINITY) ? 0.f : -m_use;
+      float rowsum = 0.f, rowsum_hat = 0.f;
+      // P as packed bf16 pairs over the first 64 columns of S (keys 2c, 2c+1 in
+      // column c); every S value is already in registers.
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t u[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int k0 = half * 64 + 2 * i;
+          const float p0 = ex2(fmaf(x[k0], sl2, neg_m));
+          const float p1 = ex2(fmaf(x[k0 + 1], sl2, neg_m));
+          u[i] = pack_bf16(p0, p1);
+          const float r0 = __uint_as_float(u[i] << 16), r1 = __uint_as_float(u[i] & 0xFFFF0000u);
+          rowsum += p0 + p1;
+          if (kPrecise) {  // keep the rounding residual for the second PV product
+            x[k0] = p0 - r0;
+            x[k0 + 1] = p1 - r1;
+          } else {
+            // O is normalised by the sum of the very weights the PV product uses
+            // (an exact convex combination of V rows); LSE uses the exact sum.
+            rowsum_hat += r0 + r1;
+          }
+        }
+        tmem_st32(s_tm + half * 32, u);
+      }
+      if (kPrecise) {  // residuals over columns 64..127 (the S values there are consumed)
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t u[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = pack_bf16(x[half * 64 + 2 * i], x[half * 64 + 2 * i + 1]);
+          tmem_st32(s_tm + 64 + half * 32, u);
+        }
+      }
+      l_run = l_run * alpha + rowsum;
+      l_hat = kPrecise ? l_run : l_hat * alpha + rowsum_hat;
+      m_run = m_use;
+      tc_fence_before();
+      mbar_arrive(&bars.p_full[t]);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && __all_sync(0xffffffffu, mbar_wait(&bars.o_full[t], 0, &bars.abort, &g_fwd_status))) {
+      tc_fence_after();
+      const float inv_l = 1.f / l_hat;
+      const size_t row_off = (static_cast<size_t>(bh) * a.N + row) * D;
+      for (int c = 0; c < D; c += 32) {
+        uint32_t u[32];
+        tmem_ld32(o_tm + c, u);
+        if (row < a.N) {
+          if (a.o_f32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.o) + row_off + c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(u[4 * i]) * inv_l, __uint_as_float(u[4 * i + 1]) * inv_l,
+                                   __uint_as_float(u[4 * i + 2]) * inv_l, __uint_as_float(u[4 * i + 3]) * inv_l);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) + row_off + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float f[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(u[8 * i + e]) * inv_l;
+              dst[i] = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                                  pack_bf16(f[6], f[7]));
+            }
+          }
+        }
+      }
+      if (row < a.N) a.lse[static_cast<size_t>(bh) * a.N + row] = (m_run + __log2f(l_run)) * kLn2;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool kPrecise>
+cudaError_t launch_fwd_t(const ForwardArgs& a, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, kPrecise>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.B * a.H, (a.N + kBM * kTiles - 1) / (kBM * kTiles));
+  fwd_kernel<D, kPrecise><<<grid, kFwdThreads, C::kSmemBytes, stream>>>(a);
+  return cudaGetLastError();
+}
+
+__global__ void wait_timeout_probe_kernel(unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, &g_fwd_status, limit_ns);  // nothing arrives
+}
+
+}  // namespace
+
+cudaError_t launch_forward(const ForwardArgs& a, cudaStream_t stream) {
+  if (a.d == 128) return a.precise ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
+  if (a.d == 64) return a.precise ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_wait_timeout_probe(unsigned long long limit_ns, cudaStream_t stream) {
+  wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(limit_ns);
+  return cudaGetLastError();
+}
+
+cudaError_t read_clear_forward_status(unsigned* out, cudaStream_t stream) {
+  cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_fwd_status, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return e;
+  const unsigned zero = 0;
+  e = cudaMemcpyToSymbolAsync(g_fwd_status, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(stream);
+}
+
+}  // namespace fa

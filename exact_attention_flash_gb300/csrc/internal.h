@@ -1,0 +1,65 @@
+// Internal launch interface shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+struct ForwardArgs {
+  CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps over [B*H, N, d] bf16, box {64, 128, 1}, 128B swizzle
+  void* o;                       // [B, H, N, d] bf16 or fp32
+  float* lse;                    // [B, H, N] natural-log log-sum-exp
+  int B, H, N, d;
+  float scale_log2;              // scale * log2(e)
+  int causal;
+  int o_f32;                     // 1: O is fp32, 0: bf16
+  int precise;                   // 1: P enters PV as a bf16 hi + lo pair (two MMAs)
+};
+
+struct BackwardArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 3-D maps over [B*H, N, d] bf16; Q, dO boxes of 64 rows, K, V of 128
+  const void* o;                        // [B, H, N, d] bf16 or fp32
+  const void* dout;                     // [B, H, N, d] bf16
+  const float* lse;                     // [B, H, N]
+  float* dq;                            // [B, H, N, d] fp32 (accumulated into; zeroed by the launcher)
+  float* dk;                            // [B, H, N, d] fp32
+  float* dv;                            // [B, H, N, d] fp32
+  float* delta;                         // [B, H, N] workspace: rowsum(dO * O)
+  int B, H, N, d;
+  float scale;                          // softmax scale
+  float scale_log2;                     // scale * log2(e)
+  int causal;
+  int o_f32;
+};
+
+struct DecodeArgs {
+  const void* q;         // [B, H, 1, d] bf16
+  const void* k;         // [B, H, L, d] bf16
+  const void* v;         // [B, H, L, d] bf16
+  float* o;              // [B, H, 1, d]
+  float* lse;            // [B, H, 1]
+  float* partials;       // optional [B, H, n_split, d + 2] (m, l, o) in natural-log units, or null
+  float* ws_partials;    // [B, H, n_split, d + 2] (m in log2 units)
+  unsigned* ws_counters; // [B, H] arrival counters, zero on entry; left at zero on exit
+  int B, H, L, d, n_split;
+  float scale_log2;
+};
+
+// Each returns a cudaError_t from the launch (cudaSuccess when queued).
+cudaError_t launch_forward(const ForwardArgs& a, cudaStream_t stream);
+cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// Device status words, one per kernel file: read and cleared on `stream`.
+cudaError_t read_clear_forward_status(unsigned* out, cudaStream_t stream);
+cudaError_t read_clear_backward_status(unsigned* out, cudaStream_t stream);
+cudaError_t read_clear_decode_status(unsigned* out, cudaStream_t stream);
+
+// Test hook: one CTA waits on an mbarrier that nothing completes, with the
+// given limit in nanoseconds; it must come back with the timeout bit set.
+cudaError_t launch_wait_timeout_probe(unsigned long long limit_ns, cudaStream_t stream);
+
+}  // namespace fa

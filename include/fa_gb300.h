@@ -1,0 +1,141 @@
+/*
+ * fa_gb300.h — C ABI of the GB300 (sm_103a) exact-attention library.
+ *
+ * The library computes exact softmax attention with tiled online softmax, its
+ * recompute backward and split-KV decoding, as defined on the web pages
+ * "attention_kernels.py" (CMU 15-779 lecture 5), "lab.py" (hs-black
+ * flash-attention post) and "flash_attention_numpy.py" (first_principles,
+ * flash-attention tier 1).
+ *
+ * Conventions for every entry point:
+ *  - Ownership: the caller owns every buffer and the stream.  The library
+ *    allocates no memory; scratch memory is passed in as `workspace`.
+ *  - Pointers are device pointers unless stated otherwise, 16-byte aligned.
+ *  - Layout: Q, K, V, O, dO, dQ, dK, dV are contiguous row-major [B, H, N, d]
+ *    (batch, head, position, feature); LSE is [B, H, N] float, natural log.
+ *  - `scale <= 0` selects the default 1/sqrt(d) ("attention_kernels.py",
+ *    section 2, ``_scale``).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Work is queued asynchronously on it.
+ *  - Errors: argument errors return synchronously (FA_ERR_INVALID_ARG,
+ *    FA_ERR_UNSUPPORTED, FA_ERR_WORKSPACE) and queue nothing.  A failed
+ *    launch returns FA_ERR_CUDA.  A kernel that hits its internal wait limit
+ *    (it never hangs) records FA_ERR_TIMEOUT, read by fa_device_status().
+ *  - Supported: d in {64, 128}; N >= 1 (any N: ragged last tiles are masked);
+ *    B * H <= 65535 * 65535.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FA_ABI_VERSION 1
+
+typedef enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null pointer, misaligned pointer, bad size */
+  FA_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. d not in {64, 128}) */
+  FA_ERR_CUDA = 3,        /* a CUDA call or launch failed */
+  FA_ERR_TIMEOUT = 4,     /* a kernel gave up waiting (reported by fa_device_status) */
+  FA_ERR_WORKSPACE = 5    /* workspace missing or smaller than the *_workspace_size() */
+} fa_status;
+
+typedef enum fa_dtype { FA_BF16 = 0, FA_F32 = 1 } fa_dtype;
+
+/* Version of this ABI (FA_ABI_VERSION of the built library). */
+int fa_abi_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* fa_status_string(fa_status s);
+
+/*
+ * fa_forward — O = softmax(Q K^T * scale [+ causal mask]) V and LSE.
+ *
+ * Defines: "attention_kernels.py" section 3 ``flash_forward`` (and section 2
+ * ``standard_attention`` for the result it must equal): S = Q K^T * scale,
+ * online softmax with running max m and denominator l rescaled by
+ * exp(m_old - m_new), O = (sum P V) / l, L = m + ln l per query row.
+ * With causal != 0, key j is visible to query i iff j <= i (q_start = 0).
+ *
+ *  q, k, v   [B, H, N, d] bf16, read only.
+ *  o         [B, H, N, d], written; o_dtype FA_BF16 or FA_F32.
+ *  lse       [B, H, N] float, written (natural log).
+ *  precise   0: P is rounded to bf16 before the P V product (standard).
+ *            1: P enters P V as a bf16 high part plus a bf16 residual (two
+ *               tensor-core products), for fp32-grade outputs.
+ * Returns FA_OK when the work is queued.
+ */
+fa_status fa_forward(const void* q, const void* k, const void* v, void* o, fa_dtype o_dtype, float* lse, int B,
+                     int H, int N, int d, float scale, int causal, int precise, void* stream);
+
+/* Bytes of workspace fa_backward needs (the row sums D = rowsum(dO * O)). */
+size_t fa_backward_workspace_size(int B, int H, int N, int d);
+
+/*
+ * fa_backward — dQ, dK, dV of loss = sum(O * dO) by recomputing P from LSE.
+ *
+ * Defines: "attention_kernels.py" section 4 ``flash_backward``:
+ * D = rowsum(dO * O); per key tile and query tile P = exp(S - L),
+ * dV += P^T dO, dP = dO V^T, dS = P * (dP - D), dQ += dS K * scale,
+ * dK += dS^T Q * scale.  The N x N matrices are never stored.
+ *
+ *  q, k, v, dout  [B, H, N, d] bf16; o [B, H, N, d] in o_dtype (the forward's
+ *                 output); lse [B, H, N] float (the forward's LSE).
+ *  dq, dk, dv     [B, H, N, d] float, written (dq is zeroed and accumulated).
+ *  workspace      device scratch of >= fa_backward_workspace_size() bytes.
+ * The causal flag and scale must match the forward call.
+ */
+fa_status fa_backward(const void* q, const void* k, const void* v, const void* o, fa_dtype o_dtype,
+                      const float* lse, const void* dout, float* dq, float* dk, float* dv, int B, int H, int N, int d,
+                      float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace fa_decode needs: per-segment states and one arrival
+ * counter per (batch, head). */
+size_t fa_decode_workspace_size(int B, int H, int d, int n_split);
+
+/*
+ * fa_decode — one query per (batch, head) against L keys, split-KV.
+ *
+ * Defines: "attention_kernels.py" section 5 ``flash_decode``: the L keys are
+ * split into n_split segments with bounds round(L * s / n_split) (ties to
+ * even), each segment yields its softmax state (m, l, o) (section 1
+ * ``SoftmaxState``), and the states are merged left to right with
+ * ``merge_states``; O = o / l.  No causal mask (the query sees every key).
+ * Segments may be empty (n_split > L) and then contribute the identity state.
+ *
+ *  q          [B, H, 1, d] bf16;  k, v  [B, H, L, d] bf16.
+ *  o          [B, H, 1, d] float, written;  lse  [B, H] float, written.
+ *  partials   optional [B, H, n_split, d + 2] float: per segment (m, l, o[d])
+ *             with m in natural-log units; NULL to skip.
+ *  workspace  device scratch of >= fa_decode_workspace_size() bytes; the call
+ *             clears the counters it holds on `stream` before the kernel runs.
+ *  n_split    >= 1 (n_split < 1 is FA_ERR_INVALID_ARG, as the page raises).
+ */
+fa_status fa_decode(const void* q, const void* k, const void* v, float* o, float* lse, int B, int H, int L, int d,
+                    float scale, int n_split, float* partials, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/*
+ * fa_device_status — synchronises `stream`, reads and clears the kernels'
+ * device status words.  Returns FA_ERR_TIMEOUT if any kernel gave up on a
+ * wait since the last call, FA_ERR_CUDA if the CUDA calls fail, else FA_OK.
+ */
+fa_status fa_device_status(void* stream);
+
+/*
+ * fa_debug_wait_timeout — test hook for the failure path: queues one CTA that
+ * waits on a barrier nothing completes, with a limit of `limit_ns`
+ * nanoseconds.  The kernel returns on its own; the next fa_device_status()
+ * must report FA_ERR_TIMEOUT.
+ */
+fa_status fa_debug_wait_timeout(unsigned long long limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

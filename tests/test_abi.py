@@ -1,0 +1,89 @@
+"""The C-ABI library builds, loads and exports every symbol its header declares;
+host-side argument checks reject bad calls before any CUDA work (CPU only)."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parent.parent
+HEADER = ROOT / "include" / "fa_gb300.h"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_flash_gb300 import _lib
+    from exact_attention_flash_gb300.build import build
+
+    build()
+    return _lib.load()
+
+
+def _declared():
+    text = re.sub(r"/\*.*?\*/", "", HEADER.read_text(), flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for required in ("fa_forward", "fa_backward", "fa_decode", "fa_device_status"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported_and_bound(lib):
+    from exact_attention_flash_gb300 import _lib
+
+    for name in _declared():
+        assert hasattr(lib, name), f"{name} not exported"
+        assert name in _lib.SIGNATURES, f"{name} has no ctypes signature"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.fa_abi_version() == 1
+    assert lib.fa_status_string(0) == b"ok"
+    assert lib.fa_status_string(4) == b"device wait timed out"
+
+
+def test_workspace_sizes(lib):
+    assert lib.fa_backward_workspace_size(2, 16, 8192, 128) == 2 * 16 * 8192 * 4
+    counters = ((16 * 32 * 4 + 255) // 256) * 256
+    partials = 16 * 32 * 64 * 130 * 4
+    assert lib.fa_decode_workspace_size(16, 32, 128, 64) == counters + ((partials + 255) // 256) * 256
+    assert lib.fa_decode_workspace_size(1, 1, 128, 0) == 0
+
+
+FAKE = 1 << 20  # a non-null, aligned pointer value; never dereferenced on these paths
+
+
+def test_forward_rejects_bad_arguments(lib):
+    assert lib.fa_forward(None, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 64, 0.0, 0, 0, None) == 1
+    assert lib.fa_forward(FAKE + 2, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 64, 0.0, 0, 0, None) == 1
+    assert lib.fa_forward(FAKE, FAKE, FAKE, FAKE, 7, FAKE, 1, 1, 8, 64, 0.0, 0, 0, None) == 1
+    assert lib.fa_forward(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 0, 64, 0.0, 0, 0, None) == 1
+    assert lib.fa_forward(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 96, 0.0, 0, 0, None) == 2
+
+
+def test_backward_rejects_bad_arguments(lib):
+    args = [FAKE] * 4 + [0, FAKE, FAKE, FAKE, FAKE, FAKE]
+    assert lib.fa_backward(*args, 1, 1, 8, 80, 0.0, 1, FAKE, 1 << 20, None) == 2
+    assert lib.fa_backward(*args, 1, 1, 8, 64, 0.0, 1, FAKE, 4, None) == 5
+    assert lib.fa_backward(*args, 1, 1, 8, 64, 0.0, 1, None, 1 << 20, None) == 5
+
+
+def test_decode_rejects_bad_arguments(lib):
+    ws = 1 << 24
+    # n_split < 1 is an error, as the page's flash_decode raises on it.
+    assert lib.fa_decode(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 128, 0.0, 0, None, FAKE, ws, None) == 1
+    assert lib.fa_decode(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 0, 128, 0.0, 4, None, FAKE, ws, None) == 1
+    assert lib.fa_decode(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 32, 0.0, 4, None, FAKE, ws, None) == 2
+    assert lib.fa_decode(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 128, 0.0, 4, None, FAKE, 8, None) == 5
+    assert lib.fa_debug_wait_timeout(0, None) == 1
+
+
+def test_python_layer_fails_loudly_without_library(monkeypatch, tmp_path):
+    from exact_attention_flash_gb300 import _lib
+
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", tmp_path / "missing.so")
+    with pytest.raises(RuntimeError, match="not built"):
+        _lib.load()

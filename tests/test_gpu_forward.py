@@ -1,0 +1,116 @@
+"""Forward parity: the sm_103a kernel through the C ABI against the float64 oracle
+on the same bf16 inputs.  Bars: O max-abs 1e-2 on the fp32 output (for a bf16
+output, 1e-2 plus bf16's own half-ulp at the reference value), LSE max-abs 2e-3,
+and 1e-4 on the precise path of the single-head N=256, d=64 forward."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention_dense, attention_dense_rows
+from tests.gpu_util import LSE_MAX_ABS, O_MAX_ABS, PRECISE_O_MAX_ABS, f64, max_abs, o_within_bar, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def _run(B, H, N, d, causal, seed, out="bf16", precise=False, mult=1.0):
+    from exact_attention_flash_gb300 import fa_device_status, fa_forward
+    from exact_attention_flash_gb300.workloads import make_attention_inputs
+
+    q, k, v, _ = make_attention_inputs(B, H, N, d, seed, "cuda", qk_mult=mult, with_do=False)
+    o, lse = fa_forward(q, k, v, causal=causal, out_dtype=DT[out], precise=precise)
+    torch.cuda.synchronize()
+    assert fa_device_status() == 0
+    return q, k, v, o, lse
+
+
+def _check(o, lse, ref_o, ref_l, out):
+    go, gl = f64(o), f64(lse)
+    assert np.isfinite(go).all() and np.isfinite(gl).all()
+    assert o_within_bar(go, ref_o, out) <= 0.0, f"O error {max_abs(go, ref_o):.3e} ({out})"
+    assert max_abs(gl, ref_l) <= LSE_MAX_ABS
+
+
+# Shapes spanning several 128-row tiles, ragged tails, a single row, and both head sizes.
+SMALL = [
+    (1, 1, 256, 64),
+    (2, 3, 300, 64),
+    (1, 2, 515, 128),
+    (2, 1, 1, 64),
+    (1, 1, 129, 128),
+    (1, 2, 1000, 128),
+    (3, 1, 640, 64),
+    (1, 1, 17, 128),
+]
+
+
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
+def test_forward_matches_oracle_small(shape, causal, out):
+    B, H, N, d = shape
+    q, k, v, o, lse = _run(B, H, N, d, causal, seed=100 + N + d, out=out)
+    ref_o, ref_l = attention_dense(f64(q), f64(k), f64(v), causal=causal)
+    _check(o, lse, ref_o, ref_l, out)
+
+
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_large_logits(causal, out):
+    """Q, K x8: scores with standard deviation about 64, nearly one-hot rows."""
+    q, k, v, o, lse = _run(2, 2, 384, 128, causal, seed=7, out=out, mult=8.0)
+    ref_o, ref_l = attention_dense(f64(q), f64(k), f64(v), causal=causal)
+    _check(o, lse, ref_o, ref_l, out)
+
+
+def test_single_head_n256_d64_fp32_paths():
+    """Seed 0, non-causal, scale 1/8, O in fp32: the precise path (P as bf16 high
+    part plus residual) is within 1e-4 of the oracle; the standard path within 1e-2."""
+    q, k, v, o_p, lse_p = _run(1, 1, 256, 64, False, seed=0, out="f32", precise=True)
+    _, _, _, o_s, lse_s = _run(1, 1, 256, 64, False, seed=0, out="f32", precise=False)
+    ref_o, ref_l = attention_dense(f64(q), f64(k), f64(v), scale=1 / 8)
+    assert max_abs(f64(o_p), ref_o) <= PRECISE_O_MAX_ABS
+    assert max_abs(f64(lse_p), ref_l) <= LSE_MAX_ABS
+    assert max_abs(f64(o_s), ref_o) <= O_MAX_ABS
+    assert max_abs(f64(lse_s), ref_l) <= LSE_MAX_ABS
+
+
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_forward_causal_b4h16_n2048_d64_full(out):
+    """Full-size causal forward (seed 1), every output compared."""
+    q, k, v, o, lse = _run(4, 16, 2048, 64, True, seed=1, out=out)
+    ref_o, ref_l = attention_dense(f64(q), f64(k), f64(v), causal=True)
+    _check(o, lse, ref_o, ref_l, out)
+
+
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_forward_causal_b2h16_n8192_d128_qk8_sampled(out):
+    """Full-size causal forward with Q, K x8 (seed 2): two whole heads compared
+    element by element, plus sampled rows of every head."""
+    q, k, v, o, lse = _run(2, 16, 8192, 128, True, seed=2, out=out, mult=8.0)
+    for b, h in [(0, 0), (1, 15)]:
+        ref_o, ref_l = attention_dense(f64(q[b, h]), f64(k[b, h]), f64(v[b, h]), causal=True)
+        _check(o[b, h], lse[b, h], ref_o, ref_l, out)
+    rows = [0, 1, 127, 128, 4095, 8190, 8191]
+    for b in range(2):
+        for h in range(16):
+            ref_o, ref_l = attention_dense_rows(f64(q[b, h]), f64(k[b, h]), f64(v[b, h]), rows, causal=True)
+            _check(o[b, h, rows], lse[b, h, rows], ref_o, ref_l, out)
+
+
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_forward_b1h32_n16384_d128_sampled(out):
+    """Full-size non-causal forward (seed 3): one whole head plus sampled rows of every head."""
+    q, k, v, o, lse = _run(1, 32, 16384, 128, False, seed=3, out=out)
+    ref_o, ref_l = attention_dense(f64(q[0, 5]), f64(k[0, 5]), f64(v[0, 5]))
+    _check(o[0, 5], lse[0, 5], ref_o, ref_l, out)
+    rows = [0, 255, 256, 9000, 16383]
+    for h in range(32):
+        ref_o, ref_l = attention_dense_rows(f64(q[0, h]), f64(k[0, h]), f64(v[0, h]), rows)
+        _check(o[0, h, rows], lse[0, h, rows], ref_o, ref_l, out)
