@@ -35,6 +35,7 @@ SIGNATURES = {
     "fa_backward": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
     "fa_decode_workspace_size": (_Z, [_I, _I, _I, _I]),
     "fa_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _Z, _P]),
+    "fa_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
     "fa_device_status": (_I, [_P]),
     "fa_debug_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
 }

@@ -21,6 +21,9 @@
 #include <cmath>
 #include <cstdint>
 
+#include <mutex>
+
+#include "../../include/fa_gb300.h"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -226,3 +229,85 @@ cudaError_t read_clear_decode_status(unsigned* out, cudaStream_t stream) {
 }
 
 }  // namespace fa
+
+// ---------------------------------------------------------------------------
+// Split-KV decode without caller-supplied scratch.
+//
+// fa_decode needs a workspace (segment states and arrival counters).  Some
+// callers cannot provide one and may not call cudaMalloc either: a plugin or
+// callback run by a host framework that owns all device memory and passes no
+// workspace, or code on a latency-critical path where cudaMalloc's implicit
+// device-wide synchronisation is not acceptable.  For them the library keeps
+// one fixed scratch array in device memory, defined below.  It exists on every
+// GPU that loads this library, for as long as the process lives.
+//
+// The array is shared by all calls: each call leaves its contents behind and
+// the next call reuses them, so calls whose work overlaps on the GPU (other
+// streams, other host threads) race on it and must be serialised by the caller.
+namespace fa {
+namespace {
+
+static __device__ __align__(256) unsigned char g_decode_static_scratch[FA_DECODE_NOALLOC_SCRATCH_BYTES];
+
+// Device address of the array, looked up once per device.  In host code the
+// array's name is only a host-side stand-in, never a device address.
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+cudaError_t static_scratch_for_current_device(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_static_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" fa_status fa_decode_noalloc(const void* q, const void* k, const void* v, float* o, float* lse, int B,
+                                       int H, int L, int d, float scale, int n_split, float* partials,
+                                       void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  const auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+  if (misaligned(q) || misaligned(k) || misaligned(v)) return FA_ERR_INVALID_ARG;
+  if (n_split < 1 || L < 1 || B < 1 || H < 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (B > 65535 || H > 65535 || n_split > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  // Same layout as the fa_decode workspace: counters (256-byte padded), then states.
+  const size_t counter_bytes = (static_cast<size_t>(B) * H * sizeof(unsigned) + 255) / 256 * 256;
+  const size_t state_bytes = static_cast<size_t>(B) * H * n_split * (d + 2) * sizeof(float);
+  if (counter_bytes + state_bytes > static_cast<size_t>(FA_DECODE_NOALLOC_SCRATCH_BYTES)) return FA_ERR_WORKSPACE;
+
+  void* scratch = nullptr;
+  if (fa::static_scratch_for_current_device(&scratch) != cudaSuccess) return FA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  fa::DecodeArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.partials = partials;
+  a.ws_counters = static_cast<unsigned*>(scratch);
+  a.ws_partials = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) + counter_bytes);
+  a.B = B;
+  a.H = H;
+  a.L = L;
+  a.d = d;
+  a.n_split = n_split;
+  a.scale_log2 = (scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(d))) * 1.4426950408889634f;
+  // The counters must start at zero; the previous call's contents are still there.
+  if (cudaMemsetAsync(a.ws_counters, 0, static_cast<size_t>(B) * H * sizeof(unsigned), s) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return fa::launch_decode(a, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}

@@ -119,6 +119,37 @@ fa_status fa_decode(const void* q, const void* k, const void* v, float* o, float
                     float scale, int n_split, float* partials, void* workspace, size_t workspace_bytes,
                     void* stream);
 
+/* Size in bytes of the fixed scratch array behind fa_decode_noalloc. */
+#define FA_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * fa_decode_noalloc — fa_decode for callers that can neither pass a workspace
+ * nor allocate device memory.  The pages have no counterpart: this is a
+ * library convenience, not part of the method.
+ *
+ * Who needs it: code that may not call cudaMalloc, for example a plugin or
+ * callback run by a framework that owns all device memory and hands it no
+ * workspace, or a latency-critical path where cudaMalloc's implicit device
+ * synchronisation is not acceptable.
+ *
+ * Same arguments, results and errors as fa_decode, minus the workspace.  The
+ * scratch memory is one fixed array of FA_DECODE_NOALLOC_SCRATCH_BYTES
+ * (16 MiB) in device memory, held by every GPU that loads the library until
+ * the process exits.  A call needs fa_decode_workspace_size(B, H, d, n_split)
+ * bytes of it and returns FA_ERR_WORKSPACE, queueing nothing, when that is
+ * larger than FA_DECODE_NOALLOC_SCRATCH_BYTES.  Nothing is allocated: no
+ * cudaMalloc, no cudaFree, no allocating library call.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the one array and each leaves
+ * its contents behind (the call clears the counters it needs on `stream`), so
+ * calls whose GPU work overlaps, on different streams or from different host
+ * threads, race with each other; serialise them.
+ */
+fa_status fa_decode_noalloc(const void* q, const void* k, const void* v, float* o, float* lse, int B, int H, int L,
+                            int d, float scale, int n_split, float* partials, void* stream);
+
 /*
  * fa_device_status — synchronises `stream`, reads and clears the kernels'
  * device status words.  Returns FA_ERR_TIMEOUT if any kernel gave up on a
