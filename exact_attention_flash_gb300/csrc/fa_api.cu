@@ -6,7 +6,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/fa_gb300.h"
+#include "fa_gb300.h"
 #include "internal.h"
 
 namespace {
@@ -101,10 +101,12 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, fa_dt
   return fa::launch_forward(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// Two fp32 arrays over [B*H, N rounded up to 64]: -LSE*log2(e) and -D per query row.
 size_t fa_backward_workspace_size(int B, int H, int N, int d) {
   (void)d;
   if (B < 1 || H < 1 || N < 1) return 0;
-  return round_up(static_cast<size_t>(B) * H * N * sizeof(float), 256);
+  const size_t n_pad = round_up(static_cast<size_t>(N), 64);
+  return 2 * round_up(static_cast<size_t>(B) * H * n_pad * sizeof(float), 256);
 }
 
 fa_status fa_backward(const void* q, const void* k, const void* v, const void* o, fa_dtype o_dtype,
@@ -131,7 +133,10 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
-  a.delta = static_cast<float*>(workspace);
+  a.n_pad = static_cast<int>(round_up(static_cast<size_t>(N), 64));
+  a.neg_lse2 = static_cast<float*>(workspace);
+  a.neg_delta = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                         round_up(static_cast<size_t>(B) * H * a.n_pad * sizeof(float), 256));
   a.B = B;
   a.H = H;
   a.N = N;

@@ -39,9 +39,16 @@ __device__ unsigned g_bwd_status;
 
 constexpr int kBKV = 128;  // keys per CTA
 constexpr int kBQ = 64;    // queries per step
-constexpr int kBwdThreads = 320;
+constexpr int kBwdThreads = 384;  // warps 10-11 only lend their registers
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+// Register split (setmaxnreg) by warpgroup: P/dS warps hold two 64-column TMEM
+// rows in registers, the dQ writer one, the producer / MMA warps little.  The
+// sum stays within the CTA's launch allocation; the launcher checks it.
+constexpr int kComputeRegs = 232;
+constexpr int kWriterRegs = 104;
+constexpr int kOtherRegs = 64;
+constexpr int kRegsNeeded = 128 * (kComputeRegs + kWriterRegs + kOtherRegs);
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -52,7 +59,9 @@ struct BwdCfg {
   static constexpr int kDSBytes = kBKV * kBQ * 2; // dS tile (bf16), 16 KB
   static constexpr int kDVCol = 256;
   static constexpr int kDKCol = 256 + D;
-  static constexpr int kSmemBytes = 2 * kKVBytes + kStages * 2 * kQBytes + 2 * kDSBytes + 1024;
+  static constexpr int kRowBytes = kBQ * 4;      // one step's -LSE*log2(e) (or -D) slice
+  static constexpr int kSmemBytes =
+      2 * kKVBytes + kStages * 2 * kQBytes + 2 * kDSBytes + kStages * 2 * kRowBytes + 1024;
 };
 
 struct BwdShared {
@@ -61,13 +70,9 @@ struct BwdShared {
   uint64_t sdp_full[2], p_full[2], dq_full[2], dq_empty[2], ds_empty[2];
   uint64_t dkdv_full;
   uint64_t drain;
-  float lse2[2][kBQ];
-  float delta[2][kBQ];
   uint32_t tmem_base;
   int abort;
 };
-
-__device__ __forceinline__ void compute_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -83,12 +88,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
   uint8_t* sQ = sV + C::kKVBytes;                       // [kStages][kQBytes]
   uint8_t* sDO = sQ + C::kStages * C::kQBytes;          // [kStages][kQBytes]
   uint8_t* sDS = sDO + C::kStages * C::kQBytes;         // [2][kDSBytes]
+  float* sNL = reinterpret_cast<float*>(sDS + 2 * C::kDSBytes);  // [kStages][kBQ] -LSE*log2(e)
+  float* sND = sNL + C::kStages * kBQ;                            // [kStages][kBQ] -D
   __shared__ BwdShared sh;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x;
-  const int j = blockIdx.y;           // key tile; small j carries the most causal work, so it starts first
+  // Head-major order: the key tiles of one head run side by side and share its
+  // Q, dO and dQ in L2; within a head, key tile 0 (the most causal work) starts first.
+  const int n_kv = (a.N + kBKV - 1) / kBKV;
+  const int bh = blockIdx.x / n_kv;
+  const int j = blockIdx.x % n_kv;
   const int key0 = j * kBKV;
   const int n_q = (a.N + kBQ - 1) / kBQ;
   const int i_start = a.causal ? key0 / kBQ : 0;
@@ -118,106 +128,116 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
 
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&a.tm_q);
-      tma_prefetch_desc(&a.tm_k);
-      tma_prefetch_desc(&a.tm_v);
-      tma_prefetch_desc(&a.tm_do);
-      mbar_arrive_expect_tx(&sh.kv_full, 2 * C::kKVBytes);
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(sK + c * (kBKV * 128), &a.tm_k, &sh.kv_full, c * 64, key0, bh);
-        tma_load_3d(sV + c * (kBKV * 128), &a.tm_v, &sh.kv_full, c * 64, key0, bh);
-      }
-      int issued = 0;
-      for (int n = 0; n < n_steps; ++n) {
-        const int s = n % C::kStages;
-        if (n >= C::kStages && !mbar_wait(&sh.q_empty[s], ((n / C::kStages) - 1) & 1, &sh.abort, &g_bwd_status))
-          break;
-        const int q0 = (i_start + n) * kBQ;
-        mbar_arrive_expect_tx(&sh.q_full[s], 2 * C::kQBytes);
+  // Each role's code sits inside the branch that set its register budget.
+  if (warp >= kProducerWarp) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
+    if (warp == kProducerWarp) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        tma_prefetch_desc(&a.tm_q);
+        tma_prefetch_desc(&a.tm_k);
+        tma_prefetch_desc(&a.tm_v);
+        tma_prefetch_desc(&a.tm_do);
+        mbar_arrive_expect_tx(&sh.kv_full, 2 * C::kKVBytes);
         for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d(sQ + s * C::kQBytes + c * (kBQ * 128), &a.tm_q, &sh.q_full[s], c * 64, q0, bh);
-          tma_load_3d(sDO + s * C::kQBytes + c * (kBQ * 128), &a.tm_do, &sh.q_full[s], c * 64, q0, bh);
+          tma_load_3d(sK + c * (kBKV * 128), &a.tm_k, &sh.kv_full, c * 64, key0, bh);
+          tma_load_3d(sV + c * (kBKV * 128), &a.tm_v, &sh.kv_full, c * 64, key0, bh);
         }
-        ++issued;
+        int issued = 0;
+        for (int n = 0; n < n_steps; ++n) {
+          const int s = n % C::kStages;
+          if (n >= C::kStages && !mbar_wait(&sh.q_empty[s], ((n / C::kStages) - 1) & 1, &sh.abort, &g_bwd_status))
+            break;
+          const int q0 = (i_start + n) * kBQ;
+          mbar_arrive_expect_tx(&sh.q_full[s], 2 * C::kQBytes + 2 * C::kRowBytes);
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_3d(sQ + s * C::kQBytes + c * (kBQ * 128), &a.tm_q, &sh.q_full[s], c * 64, q0, bh);
+            tma_load_3d(sDO + s * C::kQBytes + c * (kBQ * 128), &a.tm_do, &sh.q_full[s], c * 64, q0, bh);
+          }
+          // Row slices of the padded [B*H, n_pad] workspace arrays (always in bounds, 256-byte aligned).
+          const size_t row_off = static_cast<size_t>(bh) * a.n_pad + q0;
+          bulk_load(sNL + s * kBQ, a.neg_lse2 + row_off, C::kRowBytes, &sh.q_full[s]);
+          bulk_load(sND + s * kBQ, a.neg_delta + row_off, C::kRowBytes, &sh.q_full[s]);
+          ++issued;
+        }
+        mbar_wait_drain(&sh.kv_full, 0);
+        for (int n = max(0, issued - C::kStages); n < issued; ++n)
+          mbar_wait_drain(&sh.q_full[n % C::kStages], (n / C::kStages) & 1);
       }
-      mbar_wait_drain(&sh.kv_full, 0);
-      for (int n = max(0, issued - C::kStages); n < issued; ++n)
-        mbar_wait_drain(&sh.q_full[n % C::kStages], (n / C::kStages) & 1);
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t kIdSdP = idesc_bf16_f32(kBKV, kBQ, false, false);  // S^T, dP^T
+        constexpr uint32_t kIdKV = idesc_bf16_f32(kBKV, D, false, true);      // dV, dK (A in TMEM)
+        constexpr uint32_t kIdQ = idesc_bf16_f32(128, kBQ, true, true);       // dQ^T = K^T dS^T
+        const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aDO = smem_u32(sDO),
+                       aDS = smem_u32(sDS);
+        bool ok = mbar_wait(&sh.kv_full, 0, &sh.abort, &g_bwd_status);
+        auto issue_sdp = [&](int n) -> bool {
+          const int s = n % C::kStages, b = n & 1;
+          if (!mbar_wait(&sh.q_full[s], (n / C::kStages) & 1, &sh.abort, &g_bwd_status)) return false;
+          if (n >= 2 && !mbar_wait(&sh.dq_empty[b], ((n >> 1) - 1) & 1, &sh.abort, &g_bwd_status)) return false;
+          tc_fence_after();
+          const uint32_t q_a = aQ + s * C::kQBytes, do_a = aDO + s * C::kQBytes;
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t kv_off = (kk >> 2) * (kBKV * 128) + (kk & 3) * 32;
+            const uint32_t q_off = (kk >> 2) * (kBQ * 128) + (kk & 3) * 32;
+            umma_ss(tmem_addr(tmem, 0, b * kBQ), sdesc_sw128(aK + kv_off, 16, 1024), sdesc_sw128(q_a + q_off, 16, 1024),
+                    kIdSdP, kk > 0);
+          }
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t kv_off = (kk >> 2) * (kBKV * 128) + (kk & 3) * 32;
+            const uint32_t q_off = (kk >> 2) * (kBQ * 128) + (kk & 3) * 32;
+            umma_ss(tmem_addr(tmem, 0, 128 + b * kBQ), sdesc_sw128(aV + kv_off, 16, 1024),
+                    sdesc_sw128(do_a + q_off, 16, 1024), kIdSdP, kk > 0);
+          }
+          umma_commit(&sh.sdp_full[b]);
+          return true;
+        };
+        if (ok) {
+          tc_fence_after();
+          ok = issue_sdp(0);
+        }
+        for (int n = 0; ok && n < n_steps; ++n) {
+          const int s = n % C::kStages, b = n & 1;
+          if (n + 1 < n_steps && !issue_sdp(n + 1)) break;
+          if (!mbar_wait(&sh.p_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status)) break;
+          tc_fence_after();
+          const uint32_t q_a = aQ + s * C::kQBytes, do_a = aDO + s * C::kQBytes;
+          // dV += P^T dO_i   (K = 64 queries; dO_i is the MN-major B operand)
+  #pragma unroll
+          for (int kk = 0; kk < kBQ / 16; ++kk)
+            umma_ts(tmem_addr(tmem, 0, C::kDVCol), tmem_addr(tmem, 0, b * kBQ + kk * 8),
+                    sdesc_sw128(do_a + kk * 16 * 128, kBQ * 128, 1024), kIdKV, (n > 0 || kk > 0) ? 1u : 0u);
+          // dQ_i^T = K^T dS^T into the S^T buffer (its P^T was consumed by the dV MMA above).
+          // A = K as an MN-major [d x keys] operand; for d = 64 the upper 64 rows of the
+          // M = 128 product read the V tile and are ignored.  Issued before dK so that
+          // the dQ writer drains it while the tensor core works on dK.
+          const uint32_t ds_a = aDS + b * C::kDSBytes;
+  #pragma unroll
+          for (int kk = 0; kk < kBKV / 16; ++kk)
+            umma_ss(tmem_addr(tmem, 0, b * kBQ), sdesc_sw128(aK + kk * 16 * 128, kBKV * 128, 1024),
+                    sdesc_sw128(ds_a + kk * 16 * 128, kBKV * 128, 1024), kIdQ, kk > 0);
+          umma_commit(&sh.dq_full[b]);
+          umma_commit(&sh.ds_empty[b]);
+          // dK += dS^T Q_i
+  #pragma unroll
+          for (int kk = 0; kk < kBQ / 16; ++kk)
+            umma_ts(tmem_addr(tmem, 0, C::kDKCol), tmem_addr(tmem, 0, 128 + b * kBQ + kk * 8),
+                    sdesc_sw128(q_a + kk * 16 * 128, kBQ * 128, 1024), kIdKV, (n > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&sh.q_empty[s]);
+        }
+        if (ok) umma_commit(&sh.dkdv_full);
+        umma_commit(&sh.drain);
+        mbar_wait_drain(&sh.drain, 0);
+      }
+      __syncwarp();
     }
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdSdP = idesc_bf16_f32(kBKV, kBQ, false, false);  // S^T, dP^T
-      constexpr uint32_t kIdKV = idesc_bf16_f32(kBKV, D, false, true);      // dV, dK (A in TMEM)
-      constexpr uint32_t kIdQ = idesc_bf16_f32(128, kBQ, true, true);       // dQ^T = K^T dS^T
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aDO = smem_u32(sDO),
-                     aDS = smem_u32(sDS);
-      bool ok = mbar_wait(&sh.kv_full, 0, &sh.abort, &g_bwd_status);
-      auto issue_sdp = [&](int n) -> bool {
-        const int s = n % C::kStages, b = n & 1;
-        if (!mbar_wait(&sh.q_full[s], (n / C::kStages) & 1, &sh.abort, &g_bwd_status)) return false;
-        if (n >= 2 && !mbar_wait(&sh.dq_empty[b], ((n >> 1) - 1) & 1, &sh.abort, &g_bwd_status)) return false;
-        tc_fence_after();
-        const uint32_t q_a = aQ + s * C::kQBytes, do_a = aDO + s * C::kQBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t kv_off = (kk >> 2) * (kBKV * 128) + (kk & 3) * 32;
-          const uint32_t q_off = (kk >> 2) * (kBQ * 128) + (kk & 3) * 32;
-          umma_ss(tmem_addr(tmem, 0, b * kBQ), sdesc_sw128(aK + kv_off, 16, 1024), sdesc_sw128(q_a + q_off, 16, 1024),
-                  kIdSdP, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t kv_off = (kk >> 2) * (kBKV * 128) + (kk & 3) * 32;
-          const uint32_t q_off = (kk >> 2) * (kBQ * 128) + (kk & 3) * 32;
-          umma_ss(tmem_addr(tmem, 0, 128 + b * kBQ), sdesc_sw128(aV + kv_off, 16, 1024),
-                  sdesc_sw128(do_a + q_off, 16, 1024), kIdSdP, kk > 0);
-        }
-        umma_commit(&sh.sdp_full[b]);
-        return true;
-      };
-      if (ok) {
-        tc_fence_after();
-        ok = issue_sdp(0);
-      }
-      for (int n = 0; ok && n < n_steps; ++n) {
-        const int s = n % C::kStages, b = n & 1;
-        if (n + 1 < n_steps && !issue_sdp(n + 1)) break;
-        if (!mbar_wait(&sh.p_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status)) break;
-        tc_fence_after();
-        const uint32_t q_a = aQ + s * C::kQBytes, do_a = aDO + s * C::kQBytes;
-        // dV += P^T dO_i   (K = 64 queries; dO_i is the MN-major B operand)
-#pragma unroll
-        for (int kk = 0; kk < kBQ / 16; ++kk)
-          umma_ts(tmem_addr(tmem, 0, C::kDVCol), tmem_addr(tmem, 0, b * kBQ + kk * 8),
-                  sdesc_sw128(do_a + kk * 16 * 128, kBQ * 128, 1024), kIdKV, (n > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q_i
-#pragma unroll
-        for (int kk = 0; kk < kBQ / 16; ++kk)
-          umma_ts(tmem_addr(tmem, 0, C::kDKCol), tmem_addr(tmem, 0, 128 + b * kBQ + kk * 8),
-                  sdesc_sw128(q_a + kk * 16 * 128, kBQ * 128, 1024), kIdKV, (n > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&sh.q_empty[s]);
-        // dQ_i^T = K^T dS^T into the S^T buffer (its P^T was consumed by the dV MMA above).
-        // A = K as an MN-major [d x keys] operand; for d = 64 the upper 64 rows of the
-        // M = 128 product read the V tile and are ignored.
-        const uint32_t ds_a = aDS + b * C::kDSBytes;
-#pragma unroll
-        for (int kk = 0; kk < kBKV / 16; ++kk)
-          umma_ss(tmem_addr(tmem, 0, b * kBQ), sdesc_sw128(aK + kk * 16 * 128, kBKV * 128, 1024),
-                  sdesc_sw128(ds_a + kk * 16 * 128, kBKV * 128, 1024), kIdQ, kk > 0);
-        umma_commit(&sh.dq_full[b]);
-        umma_commit(&sh.ds_empty[b]);
-      }
-      if (ok) umma_commit(&sh.dkdv_full);
-      umma_commit(&sh.drain);
-      mbar_wait_drain(&sh.drain, 0);
-    }
-    __syncwarp();
   } else if (warp < 4) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kComputeRegs));
     // ------------------------------------------------------------ P^T and dS^T (thread = key)
     const int k = tid;
     const int key = key0 + k;
@@ -227,15 +247,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     for (int n = 0; n < n_steps; ++n) {
       const int b = n & 1;
       const int q0 = (i_start + n) * kBQ;
-      {
-        const int qq = q0 + (k & (kBQ - 1));
-        const size_t idx = static_cast<size_t>(bh) * a.N + qq;
-        if (k < kBQ)
-          sh.lse2[b][k] = (qq < a.N) ? a.lse[idx] * kLog2e : INFINITY;
-        else
-          sh.delta[b][k - kBQ] = (qq < a.N) ? a.delta[idx] : 0.f;
-      }
-      compute_bar_sync();
+      const int st = n % C::kStages;  // Q/dO stage of this step: holds its -LSE*log2(e) and -D
       if (!__all_sync(0xffffffffu, mbar_wait(&sh.sdp_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status))) {
         ok = false;
         break;
@@ -251,37 +263,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       const uint32_t s_tm = tmem_addr(tmem, lane_base, b * kBQ);
       const uint32_t dp_tm = tmem_addr(tmem, lane_base, 128 + b * kBQ);
       uint8_t* ds_row = sDS + b * C::kDSBytes + (k >> 3) * 1024 + (k & 7) * 128;
+      // One TMEM round trip in (S^T and dP^T, 64 columns each) and one out.
+      uint32_t sv[64], dpv[64];
+      tmem_ld64x2(s_tm, dp_tm, sv, dpv);
+      uint32_t pk[32], dk[32];
+      const float2 sl2x2 = make_float2(sl2, sl2);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t sv[32], dpv[32];
-        tmem_ld32(s_tm + 32 * c, sv);
-        tmem_ld32(dp_tm + 32 * c, dpv);
-        uint32_t pk[16], dk[16];
+      for (int e4 = 0; e4 < kBQ; e4 += 4) {
+        const float4 nl = *reinterpret_cast<const float4*>(sNL + st * kBQ + e4);
+        const float4 nd = *reinterpret_cast<const float4*>(sND + st * kBQ + e4);
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p[2], ds[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = 32 * c + e + u;
-            float pv = ex2(fmaf(__uint_as_float(sv[e + u]), sl2, -sh.lse2[b][col]));
-            if (need_mask && (!key_valid || q0 + col < first_visible_q)) pv = 0.f;
-            p[u] = pv;
-            ds[u] = pv * (__uint_as_float(dpv[e + u]) - sh.delta[b][col]);
+        for (int h = 0; h < 2; ++h) {
+          const int e = e4 + 2 * h;
+          const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2x2,
+                                        h == 0 ? make_float2(nl.x, nl.y) : make_float2(nl.z, nl.w));
+          float p0 = ex2(arg.x), p1 = ex2(arg.y);
+          if (need_mask) {
+            if (!key_valid || q0 + e < first_visible_q) p0 = 0.f;
+            if (!key_valid || q0 + e + 1 < first_visible_q) p1 = 0.f;
           }
-          pk[e / 2] = pack_bf16(p[0], p[1]);
-          dk[e / 2] = pack_bf16(ds[0], ds[1]);
-        }
-        tmem_st16(s_tm + 16 * c, pk);
-        tmem_st16(dp_tm + 16 * c, dk);
-        // dS^T row of this key into the MN-major, 128B-swizzled dS tile:
-        // 16-byte piece p (queries 8p..8p+7) of row k sits at ((p ^ (k & 7)) * 16).
-#pragma unroll
-        for (int pc = 0; pc < 4; ++pc) {
-          const int piece = 4 * c + pc;
-          *reinterpret_cast<uint4*>(ds_row + ((piece ^ (k & 7)) << 4)) =
-              make_uint4(dk[4 * pc], dk[4 * pc + 1], dk[4 * pc + 2], dk[4 * pc + 3]);
+          const float2 ds2 =
+              __fmul2_rn(make_float2(p0, p1),
+                         __fadd2_rn(make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])),
+                                    h == 0 ? make_float2(nd.x, nd.y) : make_float2(nd.z, nd.w)));
+          pk[e / 2] = pack_bf16(p0, p1);
+          dk[e / 2] = pack_bf16(ds2.x, ds2.y);
         }
       }
+      // dS^T row of this key into the MN-major, 128B-swizzled dS tile:
+      // 16-byte piece p (queries 8p..8p+7) of row k sits at ((p ^ (k & 7)) * 16).
+#pragma unroll
+      for (int piece = 0; piece < 8; ++piece)
+        *reinterpret_cast<uint4*>(ds_row + ((piece ^ (k & 7)) << 4)) =
+            make_uint4(dk[4 * piece], dk[4 * piece + 1], dk[4 * piece + 2], dk[4 * piece + 3]);
+      tmem_st32x2(s_tm, pk, dp_tm, dk);
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(&sh.p_full[b]);
@@ -309,6 +324,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       }
     }
   } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kWriterRegs));
     // ------------------------------------------------------------ dQ writer (thread = feature)
     const int c = tid - 128;                 // feature index == TMEM lane of dQ^T
     const int lane_base = (warp & 3) * 32;
@@ -340,16 +356,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
   }
 }
 
-// One warp per query row: D = rowsum(dO * O) and dQ := 0 for the row.
+// One warp per row of the padded [B*H, n_pad] layout.  Rows q < N: -D with
+// D = rowsum(dO * O), -LSE * log2(e), and dQ := 0.  Padding rows q >= N: -inf and 0,
+// so that a query past the end contributes P = 0.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess(const void* __restrict__ o, int o_f32,
                                                        const __nv_bfloat16* __restrict__ dout,
-                                                       float* __restrict__ delta, float* __restrict__ dq,
-                                                       long long rows) {
+                                                       const float* __restrict__ lse, float* __restrict__ neg_lse2,
+                                                       float* __restrict__ neg_delta, float* __restrict__ dq, int N,
+                                                       int n_pad, long long padded_rows) {
   constexpr int kPer = D / 32;
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const long long prow = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
+  if (prow >= padded_rows) return;
+  const long long bh = prow / n_pad;
+  const int q = static_cast<int>(prow - bh * n_pad);
+  if (q >= N) {
+    if (lane == 0) {
+      neg_lse2[prow] = -INFINITY;
+      neg_delta[prow] = 0.f;
+    }
+    return;
+  }
+  const long long row = bh * N + q;
   const size_t base = static_cast<size_t>(row) * D + lane * kPer;
   float acc = 0.f;
 #pragma unroll
@@ -361,20 +390,32 @@ __global__ void __launch_bounds__(256) bwd_preprocess(const void* __restrict__ o
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) delta[row] = acc;
+  if (lane == 0) {
+    neg_delta[prow] = -acc;
+    neg_lse2[prow] = -lse[row] * kLog2e;
+  }
 }
 
 template <int D>
 cudaError_t launch_bwd_t(const BackwardArgs& a, cudaStream_t stream) {
   using C = BwdCfg<D>;
-  const long long rows = static_cast<long long>(a.B) * a.H * a.N;
-  bwd_preprocess<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-      a.o, a.o_f32, static_cast<const __nv_bfloat16*>(a.dout), a.delta, a.dq, rows);
+  const long long padded_rows = static_cast<long long>(a.B) * a.H * a.n_pad;
+  bwd_preprocess<D><<<static_cast<unsigned>((padded_rows + 7) / 8), 256, 0, stream>>>(
+      a.o, a.o_f32, static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.neg_lse2, a.neg_delta, a.dq, a.N, a.n_pad,
+      padded_rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.B * a.H, (a.N + kBKV - 1) / kBKV);
+  // The setmaxnreg split is granted from the CTA's launch allocation; refuse to
+  // launch rather than let a raise wait for registers that do not exist.
+  cudaFuncAttributes attr{};
+  e = cudaFuncGetAttributes(&attr, bwd_kernel<D>);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs * kBwdThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
+  const long long ctas = static_cast<long long>(a.B) * a.H * ((a.N + kBKV - 1) / kBKV);
+  if (ctas > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  dim3 grid(static_cast<unsigned>(ctas));
   bwd_kernel<D><<<grid, kBwdThreads, C::kSmemBytes, stream>>>(a);
   return cudaGetLastError();
 }

@@ -23,7 +23,7 @@
 
 #include <mutex>
 
-#include "../../include/fa_gb300.h"
+#include "fa_gb300.h"
 #include "internal.h"
 #include "ptx.cuh"
 

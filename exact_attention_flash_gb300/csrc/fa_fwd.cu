@@ -42,7 +42,13 @@ constexpr int kBN = 128;             // keys per KV tile
 constexpr int kTiles = 2;            // query tiles per CTA
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kFwdThreads = 320;
+constexpr int kFwdThreads = 384;  // warps 10-11 only lend their registers to the softmax warps
+// Register split (setmaxnreg): softmax warpgroups 0-1 raise their budget, warpgroup 2
+// (producer, MMA issuer, two idle warps) lowers it.  The sum must stay within what
+// the CTA was launched with; the launcher checks this against the compiled kernel.
+constexpr int kSoftmaxRegs = 216;
+constexpr int kOtherRegs = 64;
+constexpr int kRegsNeeded = 256 * kSoftmaxRegs + 128 * kOtherRegs;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -76,8 +82,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x;
-  const int q_row0 = (gridDim.y - 1 - blockIdx.y) * (kBM * kTiles);  // heaviest query blocks first
+  // Head-major order: the query blocks of one head run side by side and share
+  // its K and V in L2; within a head the heaviest (latest) causal block starts first.
+  const int n_qblk = (a.N + kBM * kTiles - 1) / (kBM * kTiles);
+  const int bh = blockIdx.x / n_qblk;
+  const int q_row0 = (n_qblk - 1 - static_cast<int>(blockIdx.x % n_qblk)) * (kBM * kTiles);
   const int n_kv_total = (a.N + kBN - 1) / kBN;
   int n_kv[kTiles];
 #pragma unroll
@@ -107,114 +116,120 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
 
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&a.tm_q);
-      tma_prefetch_desc(&a.tm_k);
-      tma_prefetch_desc(&a.tm_v);
-      mbar_arrive_expect_tx(&bars.q_full, kTiles * C::kTileBytes);
-      for (int t = 0; t < kTiles; ++t)
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(sQ + t * C::kTileBytes + c * (kBM * 128), &a.tm_q, &bars.q_full, c * 64, q_row0 + t * kBM, bh);
-      int issued = 0;
-      for (int j = 0; j < n_kv_cta; ++j) {
-        const int s = j % C::kStages;
-        if (j >= C::kStages && !mbar_wait(&bars.kv_empty[s], ((j / C::kStages) - 1) & 1, &bars.abort, &g_fwd_status))
-          break;
-        uint8_t* k_dst = sK + s * C::kTileBytes;
-        uint8_t* v_dst = sV + s * C::kTileBytes;
-        mbar_arrive_expect_tx(&bars.k_full[s], C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(k_dst + c * (kBN * 128), &a.tm_k, &bars.k_full[s], c * 64, j * kBN, bh);
-        mbar_arrive_expect_tx(&bars.v_full[s], C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(v_dst + c * (kBN * 128), &a.tm_v, &bars.v_full[s], c * 64, j * kBN, bh);
-        ++issued;
-      }
-      // Drain: every copy this CTA started must land before shared memory is released.
-      mbar_wait_drain(&bars.q_full, 0);
-      for (int j = max(0, issued - C::kStages); j < issued; ++j) {
-        const int s = j % C::kStages;
-        mbar_wait_drain(&bars.k_full[s], (j / C::kStages) & 1);
-        mbar_wait_drain(&bars.v_full[s], (j / C::kStages) & 1);
-      }
-    }
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, false, false);
-      constexpr uint32_t kIdO = idesc_bf16_f32(kBM, D, false, true);
-      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
-      auto issue_s = [&](int t, int j) {
-        const int s = j % C::kStages;
-        const uint32_t qa = sQa + t * C::kTileBytes, ka = sKa + s * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-          umma_ss(tmem_addr(tmem, 0, t * kBN), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                  kIdS, kk > 0);
+  // Each role's code sits inside the branch that set its register budget (the
+  // compiler applies a budget to the code it dominates).
+  if (warp >= kProducerWarp) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
+    if (warp == kProducerWarp) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        tma_prefetch_desc(&a.tm_q);
+        tma_prefetch_desc(&a.tm_k);
+        tma_prefetch_desc(&a.tm_v);
+        mbar_arrive_expect_tx(&bars.q_full, kTiles * C::kTileBytes);
+        for (int t = 0; t < kTiles; ++t)
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(sQ + t * C::kTileBytes + c * (kBM * 128), &a.tm_q, &bars.q_full, c * 64, q_row0 + t * kBM, bh);
+        int issued = 0;
+        for (int j = 0; j < n_kv_cta; ++j) {
+          const int s = j % C::kStages;
+          if (j >= C::kStages && !mbar_wait(&bars.kv_empty[s], ((j / C::kStages) - 1) & 1, &bars.abort, &g_fwd_status))
+            break;
+          uint8_t* k_dst = sK + s * C::kTileBytes;
+          uint8_t* v_dst = sV + s * C::kTileBytes;
+          mbar_arrive_expect_tx(&bars.k_full[s], C::kTileBytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(k_dst + c * (kBN * 128), &a.tm_k, &bars.k_full[s], c * 64, j * kBN, bh);
+          mbar_arrive_expect_tx(&bars.v_full[s], C::kTileBytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(v_dst + c * (kBN * 128), &a.tm_v, &bars.v_full[s], c * 64, j * kBN, bh);
+          ++issued;
         }
-        umma_commit(&bars.s_full[t]);
-      };
-      auto issue_pv = [&](int t, int j) {
-        const int s = j % C::kStages;
-        const uint32_t va = sVa + s * C::kTileBytes;
-        const uint32_t o_tm = tmem_addr(tmem, 0, C::kOCol + t * D);
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_ts(o_tm, tmem_addr(tmem, 0, t * kBN + kk * 8), sdesc_sw128(va + kk * 16 * 128, kBN * 128, 1024), kIdO,
-                  (j > 0 || kk > 0) ? 1u : 0u);
-        if (kPrecise) {
-#pragma unroll
+        // Drain: every copy this CTA started must land before shared memory is released.
+        mbar_wait_drain(&bars.q_full, 0);
+        for (int j = max(0, issued - C::kStages); j < issued; ++j) {
+          const int s = j % C::kStages;
+          mbar_wait_drain(&bars.k_full[s], (j / C::kStages) & 1);
+          mbar_wait_drain(&bars.v_full[s], (j / C::kStages) & 1);
+        }
+      }
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, false, false);
+        constexpr uint32_t kIdO = idesc_bf16_f32(kBM, D, false, true);
+        const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+        auto issue_s = [&](int t, int j) {
+          const int s = j % C::kStages;
+          const uint32_t qa = sQa + t * C::kTileBytes, ka = sKa + s * C::kTileBytes;
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+            umma_ss(tmem_addr(tmem, 0, t * kBN), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                    kIdS, kk > 0);
+          }
+          umma_commit(&bars.s_full[t]);
+        };
+        auto issue_pv = [&](int t, int j) {
+          const int s = j % C::kStages;
+          const uint32_t va = sVa + s * C::kTileBytes;
+          const uint32_t o_tm = tmem_addr(tmem, 0, C::kOCol + t * D);
+  #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
-            umma_ts(o_tm, tmem_addr(tmem, 0, t * kBN + 64 + kk * 8), sdesc_sw128(va + kk * 16 * 128, kBN * 128, 1024),
-                    kIdO, 1u);
-        }
-      };
-      bool ok = mbar_wait(&bars.q_full, 0, &bars.abort, &g_fwd_status) &&
-                mbar_wait(&bars.k_full[0], 0, &bars.abort, &g_fwd_status);
-      if (ok) {
-        tc_fence_after();
-        for (int t = 0; t < kTiles; ++t) issue_s(t, 0);
-      }
-      for (int j = 0; ok && j < n_kv_cta; ++j) {
-        const int s = j % C::kStages;
-        const int jn = j + 1, sn = jn % C::kStages;
-        if (!mbar_wait(&bars.v_full[s], (j / C::kStages) & 1, &bars.abort, &g_fwd_status)) break;
-        // tile 0
-        if (j < n_kv[0]) {
-          if (!mbar_wait(&bars.p_full[0], j & 1, &bars.abort, &g_fwd_status)) break;
+            umma_ts(o_tm, tmem_addr(tmem, 0, t * kBN + kk * 8), sdesc_sw128(va + kk * 16 * 128, kBN * 128, 1024), kIdO,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+          if (kPrecise) {
+  #pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              umma_ts(o_tm, tmem_addr(tmem, 0, t * kBN + 64 + kk * 8), sdesc_sw128(va + kk * 16 * 128, kBN * 128, 1024),
+                      kIdO, 1u);
+          }
+        };
+        bool ok = mbar_wait(&bars.q_full, 0, &bars.abort, &g_fwd_status) &&
+                  mbar_wait(&bars.k_full[0], 0, &bars.abort, &g_fwd_status);
+        if (ok) {
           tc_fence_after();
-          issue_pv(0, j);
-          if (jn < n_kv[0]) {
+          for (int t = 0; t < kTiles; ++t) issue_s(t, 0);
+        }
+        for (int j = 0; ok && j < n_kv_cta; ++j) {
+          const int s = j % C::kStages;
+          const int jn = j + 1, sn = jn % C::kStages;
+          if (!mbar_wait(&bars.v_full[s], (j / C::kStages) & 1, &bars.abort, &g_fwd_status)) break;
+          // tile 0
+          if (j < n_kv[0]) {
+            if (!mbar_wait(&bars.p_full[0], j & 1, &bars.abort, &g_fwd_status)) break;
+            tc_fence_after();
+            issue_pv(0, j);
+            if (jn < n_kv[0]) {
+              if (!mbar_wait(&bars.k_full[sn], (jn / C::kStages) & 1, &bars.abort, &g_fwd_status)) break;
+              tc_fence_after();
+              issue_s(0, jn);
+            } else {
+              umma_commit(&bars.o_full[0]);
+            }
+          }
+          // tile 1
+          if (!mbar_wait(&bars.p_full[1], j & 1, &bars.abort, &g_fwd_status)) break;
+          tc_fence_after();
+          issue_pv(1, j);
+          umma_commit(&bars.kv_empty[s]);
+          if (jn < n_kv[1]) {
             if (!mbar_wait(&bars.k_full[sn], (jn / C::kStages) & 1, &bars.abort, &g_fwd_status)) break;
             tc_fence_after();
-            issue_s(0, jn);
+            issue_s(1, jn);
           } else {
-            umma_commit(&bars.o_full[0]);
+            umma_commit(&bars.o_full[1]);
           }
         }
-        // tile 1
-        if (!mbar_wait(&bars.p_full[1], j & 1, &bars.abort, &g_fwd_status)) break;
-        tc_fence_after();
-        issue_pv(1, j);
-        umma_commit(&bars.kv_empty[s]);
-        if (jn < n_kv[1]) {
-          if (!mbar_wait(&bars.k_full[sn], (jn / C::kStages) & 1, &bars.abort, &g_fwd_status)) break;
-          tc_fence_after();
-          issue_s(1, jn);
-        } else {
-          umma_commit(&bars.o_full[1]);
-        }
+        // Drain: all MMAs complete before tensor memory is released.
+        umma_commit(&bars.drain);
+        mbar_wait_drain(&bars.drain, 0);
       }
-      // Drain: all MMAs complete before tensor memory is released.
-      umma_commit(&bars.drain);
-      mbar_wait_drain(&bars.drain, 0);
+      __syncwarp();
     }
-    __syncwarp();
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;                  // query tile of this warpgroup
     const int r = tid - t * kBM;              // row within the tile == TMEM lane
@@ -252,9 +267,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         for (int i = 0; i < kBN; ++i)
           if (key0 + i > lim) x[i] = -INFINITY;
       }
-      float mx = x[0];
+      // Row max as eight independent chains of 3-input maxima (short dependency paths).
+      float mx8[8];
 #pragma unroll
-      for (int i = 1; i < kBN; ++i) mx = fmaxf(mx, x[i]);
+      for (int c = 0; c < 8; ++c) {
+        float v = fmax3(x[16 * c], x[16 * c + 1], x[16 * c + 2]);
+#pragma unroll
+        for (int i = 3; i < 15; i += 2) v = fmax3(v, x[16 * c + i], x[16 * c + i + 1]);
+        mx8[c] = fmaxf(v, x[16 * c + 15]);
+      }
+      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
       const float m_tile = mx * sl2;
       float m_use = m_run;
       float alpha = 1.f;
@@ -274,7 +296,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         }
       }
       const float neg_m = (m_use == -INFINITY) ? 0.f : -m_use;
-      float rowsum = 0.f, rowsum_hat = 0.f;
+      const float2 sl2x2 = make_float2(sl2, sl2), negm2 = make_float2(neg_m, neg_m);
+      float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       // P as packed bf16 pairs over the first 64 columns of S (keys 2c, 2c+1 in
       // column c); every S value is already in registers.
 #pragma unroll
@@ -283,18 +306,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int k0 = half * 64 + 2 * i;
-          const float p0 = ex2(fmaf(x[k0], sl2, neg_m));
-          const float p1 = ex2(fmaf(x[k0 + 1], sl2, neg_m));
+          const float2 e = __ffma2_rn(make_float2(x[k0], x[k0 + 1]), sl2x2, negm2);
+          const float p0 = ex2(e.x), p1 = ex2(e.y);
           u[i] = pack_bf16(p0, p1);
-          const float r0 = __uint_as_float(u[i] << 16), r1 = __uint_as_float(u[i] & 0xFFFF0000u);
-          rowsum += p0 + p1;
+          sum2[i & 3] = __fadd2_rn(sum2[i & 3], make_float2(p0, p1));
           if (kPrecise) {  // keep the rounding residual for the second PV product
-            x[k0] = p0 - r0;
-            x[k0 + 1] = p1 - r1;
-          } else {
-            // O is normalised by the sum of the very weights the PV product uses
-            // (an exact convex combination of V rows); LSE uses the exact sum.
-            rowsum_hat += r0 + r1;
+            x[k0] = p0 - __uint_as_float(u[i] << 16);
+            x[k0 + 1] = p1 - __uint_as_float(u[i] & 0xFFFF0000u);
           }
         }
         tmem_st32(s_tm + half * 32, u);
@@ -308,8 +326,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           tmem_st32(s_tm + 64 + half * 32, u);
         }
       }
+      const float2 s01 = __fadd2_rn(sum2[0], sum2[1]), s23 = __fadd2_rn(sum2[2], sum2[3]);
+      const float2 s4 = __fadd2_rn(s01, s23);
+      const float rowsum = s4.x + s4.y;
+      // Normaliser of O.  P enters the PV product rounded to bf16.  With the
+      // reference max held back (lazy rescaling) the row's largest weight is
+      // 2^(x_max - m) <= 2^8 instead of exactly 1, and its rounding error would
+      // bias O by up to 2^-9 of a V row.  Adding that one element's rounding
+      // error to the exact sum removes the bias; the other weights' rounding
+      // errors are bounded and unbiased as in the standard bf16-P scheme.
+      // (The same fused multiply-add and ex2 on the same input reproduce the
+      // loop's value of that element bit for bit.)
+      float delta_max = 0.f;
+      if (!kPrecise) {
+        const float p_max = ex2(fmaf(mx, sl2, neg_m));
+        delta_max = __uint_as_float(pack_bf16(p_max, 0.f) << 16) - p_max;
+      }
       l_run = l_run * alpha + rowsum;
-      l_hat = kPrecise ? l_run : l_hat * alpha + rowsum_hat;
+      l_hat = kPrecise ? l_run : l_hat * alpha + (rowsum + delta_max);
       m_run = m_use;
       tc_fence_before();
       mbar_arrive(&bars.p_full[t]);
@@ -360,7 +394,15 @@ cudaError_t launch_fwd_t(const ForwardArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, kPrecise>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.B * a.H, (a.N + kBM * kTiles - 1) / (kBM * kTiles));
+  // The setmaxnreg split can only be granted from the registers the CTA is
+  // launched with; refuse to launch rather than let the raise wait forever.
+  cudaFuncAttributes attr{};
+  e = cudaFuncGetAttributes(&attr, fwd_kernel<D, kPrecise>);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs * kFwdThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
+  const long long ctas = static_cast<long long>(a.B) * a.H * ((a.N + kBM * kTiles - 1) / (kBM * kTiles));
+  if (ctas > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  dim3 grid(static_cast<unsigned>(ctas));
   fwd_kernel<D, kPrecise><<<grid, kFwdThreads, C::kSmemBytes, stream>>>(a);
   return cudaGetLastError();
 }

@@ -27,7 +27,9 @@ struct BackwardArgs {
   float* dq;                            // [B, H, N, d] fp32 (accumulated into; zeroed by the launcher)
   float* dk;                            // [B, H, N, d] fp32
   float* dv;                            // [B, H, N, d] fp32
-  float* delta;                         // [B, H, N] workspace: rowsum(dO * O)
+  float* neg_lse2;                      // workspace [B*H, n_pad]: -LSE * log2(e), -inf past N
+  float* neg_delta;                     // workspace [B*H, n_pad]: -rowsum(dO * O), 0 past N
+  int n_pad;                            // N rounded up to a multiple of 64
   int B, H, N, d;
   float scale;                          // softmax scale
   float scale_log2;                     // scale * log2(e)
