@@ -20,7 +20,7 @@
 //   dP^T into P^T, dS^T, warps 4-7 (thread = feature) add dQ_i^T into dQ with
 //   fp32 reductions in L2.  S^T/dP^T are double-buffered in TMEM so the tensor
 //   core computes step n+1 while step n's elementwise work runs; dQ^T of step
-//   n lands in the S^T buffer that P^T of step n has just left.
+//   n lands in the dP^T buffer that dS^T of step n has just left.
 // Tensor memory (512 columns): S^T[2] [0,64) [64,128), dP^T[2] [128,192)
 // [192,256), dV [256, 256+d), dK [256+d, 256+2d).
 #include <cuda_bf16.h>
@@ -39,16 +39,20 @@ __device__ unsigned g_bwd_status;
 
 constexpr int kBKV = 128;  // keys per CTA
 constexpr int kBQ = 64;    // queries per step
-constexpr int kBwdThreads = 384;  // warps 10-11 only lend their registers
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+// Warps 0-3: P^T / dS^T; warps 4-11: dQ writers (two warpgroups, one per half of
+// the step's 64 query columns); warp 12: TMA producer; warp 13: MMA issuer;
+// warps 14-15 only lend their registers.
+constexpr int kBwdThreads = 512;
+constexpr int kWriterWarp0 = 4;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
 // Register split (setmaxnreg) by warpgroup: P/dS warps hold two 64-column TMEM
-// rows in registers, the dQ writer one, the producer / MMA warps little.  The
-// sum stays within the CTA's launch allocation; the launcher checks it.
+// rows in registers, each dQ writer one 32-column row, the producer / MMA warps
+// little.  The sum stays within the CTA's launch allocation; the launcher checks it.
 constexpr int kComputeRegs = 232;
-constexpr int kWriterRegs = 104;
-constexpr int kOtherRegs = 64;
-constexpr int kRegsNeeded = 128 * (kComputeRegs + kWriterRegs + kOtherRegs);
+constexpr int kWriterRegs = 64;
+constexpr int kOtherRegs = 88;
+constexpr int kRegsNeeded = 128 * kComputeRegs + 256 * kWriterRegs + 128 * kOtherRegs;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -73,6 +77,10 @@ struct BwdShared {
   uint32_t tmem_base;
   int abort;
 };
+
+// Advance a shared-memory descriptor's start address by `bytes` (a multiple of 16
+// that keeps the address inside the same 256 KB window).
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -115,7 +123,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       mbar_init(&sh.sdp_full[b], 1);
       mbar_init(&sh.p_full[b], 128);
       mbar_init(&sh.dq_full[b], 1);
-      mbar_init(&sh.dq_empty[b], 128);
+      mbar_init(&sh.dq_empty[b], 256);
       mbar_init(&sh.ds_empty[b], 1);
     }
     mbar_init(&sh.dkdv_full, 1);
@@ -171,29 +179,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         constexpr uint32_t kIdSdP = idesc_bf16_f32(kBKV, kBQ, false, false);  // S^T, dP^T
         constexpr uint32_t kIdKV = idesc_bf16_f32(kBKV, D, false, true);      // dV, dK (A in TMEM)
         constexpr uint32_t kIdQ = idesc_bf16_f32(128, kBQ, true, true);       // dQ^T = K^T dS^T
-        const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aDO = smem_u32(sDO),
-                       aDS = smem_u32(sDS);
+        // Descriptors are built once; each MMA only adds a constant offset (a short
+        // issue path matters: the tensor core's queue is shallow).
+        const uint64_t dK_k = sdesc_sw128(smem_u32(sK), 16, 1024);          // K, K-major (A of S^T)
+        const uint64_t dV_k = sdesc_sw128(smem_u32(sV), 16, 1024);          // V, K-major (A of dP^T)
+        const uint64_t dK_mn = sdesc_sw128(smem_u32(sK), kBKV * 128, 1024); // K as MN-major A of dQ^T
+        const uint64_t dQ_k = sdesc_sw128(smem_u32(sQ), 16, 1024);          // Q stage 0, K-major (B of S^T)
+        const uint64_t dDO_k = sdesc_sw128(smem_u32(sDO), 16, 1024);        // dO stage 0, K-major (B of dP^T)
+        const uint64_t dQ_mn = sdesc_sw128(smem_u32(sQ), kBQ * 128, 1024);  // Q stage 0, MN-major (B of dK)
+        const uint64_t dDO_mn = sdesc_sw128(smem_u32(sDO), kBQ * 128, 1024);// dO stage 0, MN-major (B of dV)
+        const uint64_t dDS_mn = sdesc_sw128(smem_u32(sDS), kBKV * 128, 1024);// dS buffer 0, MN-major (B of dQ^T)
         bool ok = mbar_wait(&sh.kv_full, 0, &sh.abort, &g_bwd_status);
+        // S^T(n) and dP^T(n) into buffer n & 1.  The S^T buffer's previous user (P^T of
+        // step n - 2, read by dV) is done by issue order; the dP^T buffer also held
+        // dQ^T of step n - 2, so the dQ writers must have drained it first.  S^T goes
+        // first so that its products cover that hand-off.
         auto issue_sdp = [&](int n) -> bool {
           const int s = n % C::kStages, b = n & 1;
           if (!mbar_wait(&sh.q_full[s], (n / C::kStages) & 1, &sh.abort, &g_bwd_status)) return false;
+          tc_fence_after();
+          const uint64_t q_d = desc_add(dQ_k, s * C::kQBytes), do_d = desc_add(dDO_k, s * C::kQBytes);
+          const uint32_t s_tm = tmem + b * kBQ;
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(s_tm, desc_add(dK_k, (kk >> 2) * (kBKV * 128) + (kk & 3) * 32),
+                    desc_add(q_d, (kk >> 2) * (kBQ * 128) + (kk & 3) * 32), kIdSdP, kk > 0);
           if (n >= 2 && !mbar_wait(&sh.dq_empty[b], ((n >> 1) - 1) & 1, &sh.abort, &g_bwd_status)) return false;
           tc_fence_after();
-          const uint32_t q_a = aQ + s * C::kQBytes, do_a = aDO + s * C::kQBytes;
   #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t kv_off = (kk >> 2) * (kBKV * 128) + (kk & 3) * 32;
-            const uint32_t q_off = (kk >> 2) * (kBQ * 128) + (kk & 3) * 32;
-            umma_ss(tmem_addr(tmem, 0, b * kBQ), sdesc_sw128(aK + kv_off, 16, 1024), sdesc_sw128(q_a + q_off, 16, 1024),
-                    kIdSdP, kk > 0);
-          }
-  #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t kv_off = (kk >> 2) * (kBKV * 128) + (kk & 3) * 32;
-            const uint32_t q_off = (kk >> 2) * (kBQ * 128) + (kk & 3) * 32;
-            umma_ss(tmem_addr(tmem, 0, 128 + b * kBQ), sdesc_sw128(aV + kv_off, 16, 1024),
-                    sdesc_sw128(do_a + q_off, 16, 1024), kIdSdP, kk > 0);
-          }
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(s_tm + 128, desc_add(dV_k, (kk >> 2) * (kBKV * 128) + (kk & 3) * 32),
+                    desc_add(do_d, (kk >> 2) * (kBQ * 128) + (kk & 3) * 32), kIdSdP, kk > 0);
           umma_commit(&sh.sdp_full[b]);
           return true;
         };
@@ -206,29 +222,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
           if (n + 1 < n_steps && !issue_sdp(n + 1)) break;
           if (!mbar_wait(&sh.p_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status)) break;
           tc_fence_after();
-          const uint32_t q_a = aQ + s * C::kQBytes, do_a = aDO + s * C::kQBytes;
+          const uint64_t q_d = desc_add(dQ_mn, s * C::kQBytes), do_d = desc_add(dDO_mn, s * C::kQBytes);
+          const uint32_t s_tm = tmem + b * kBQ;
+          const uint32_t acc0 = n > 0 ? 1u : 0u;
           // dV += P^T dO_i   (K = 64 queries; dO_i is the MN-major B operand)
   #pragma unroll
           for (int kk = 0; kk < kBQ / 16; ++kk)
-            umma_ts(tmem_addr(tmem, 0, C::kDVCol), tmem_addr(tmem, 0, b * kBQ + kk * 8),
-                    sdesc_sw128(do_a + kk * 16 * 128, kBQ * 128, 1024), kIdKV, (n > 0 || kk > 0) ? 1u : 0u);
-          // dQ_i^T = K^T dS^T into the S^T buffer (its P^T was consumed by the dV MMA above).
-          // A = K as an MN-major [d x keys] operand; for d = 64 the upper 64 rows of the
-          // M = 128 product read the V tile and are ignored.  Issued before dK so that
-          // the dQ writer drains it while the tensor core works on dK.
-          const uint32_t ds_a = aDS + b * C::kDSBytes;
-  #pragma unroll
-          for (int kk = 0; kk < kBKV / 16; ++kk)
-            umma_ss(tmem_addr(tmem, 0, b * kBQ), sdesc_sw128(aK + kk * 16 * 128, kBKV * 128, 1024),
-                    sdesc_sw128(ds_a + kk * 16 * 128, kBKV * 128, 1024), kIdQ, kk > 0);
-          umma_commit(&sh.dq_full[b]);
-          umma_commit(&sh.ds_empty[b]);
+            umma_ts(tmem + C::kDVCol, s_tm + kk * 8, desc_add(do_d, kk * 16 * 128), kIdKV, kk > 0 ? 1u : acc0);
           // dK += dS^T Q_i
   #pragma unroll
           for (int kk = 0; kk < kBQ / 16; ++kk)
-            umma_ts(tmem_addr(tmem, 0, C::kDKCol), tmem_addr(tmem, 0, 128 + b * kBQ + kk * 8),
-                    sdesc_sw128(q_a + kk * 16 * 128, kBQ * 128, 1024), kIdKV, (n > 0 || kk > 0) ? 1u : 0u);
+            umma_ts(tmem + C::kDKCol, s_tm + 128 + kk * 8, desc_add(q_d, kk * 16 * 128), kIdKV, kk > 0 ? 1u : acc0);
           umma_commit(&sh.q_empty[s]);
+          // dQ_i^T = K^T dS^T into the dP^T buffer (its dS^T was consumed by the dK MMA above).
+          // A = K as an MN-major [d x keys] operand; for d = 64 the upper 64 rows of the
+          // M = 128 product read the V tile and are ignored.
+          const uint64_t ds_d = desc_add(dDS_mn, b * C::kDSBytes);
+  #pragma unroll
+          for (int kk = 0; kk < kBKV / 16; ++kk)
+            umma_ss(s_tm + 128, desc_add(dK_mn, kk * 16 * 128), desc_add(ds_d, kk * 16 * 128), kIdQ, kk > 0);
+          umma_commit(&sh.dq_full[b]);
+          umma_commit(&sh.ds_empty[b]);
         }
         if (ok) umma_commit(&sh.dkdv_full);
         umma_commit(&sh.drain);
@@ -325,24 +339,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     }
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kWriterRegs));
-    // ------------------------------------------------------------ dQ writer (thread = feature)
-    const int c = tid - 128;                 // feature index == TMEM lane of dQ^T
+    // ------------------------------------------------------------ dQ writers (thread = feature)
+    // dQ_i^T sits in TMEM with one feature per lane and one query per column.  Each
+    // writer warpgroup takes 32 of the 64 query columns and adds them into dQ with
+    // fp32 reductions in L2 (a warp's 32 lanes cover 128 contiguous bytes of a row).
+    const int half = (warp - kWriterWarp0) >> 2;  // query columns [32*half, 32*half + 32)
     const int lane_base = (warp & 3) * 32;
-    const bool has_rows = lane_base < D;     // for d = 64, lanes 64..127 hold no feature
+    const int c = lane_base + lane;               // feature index == TMEM lane of dQ^T
+    const bool has_rows = lane_base < D;          // for d = 64, lanes 64..127 hold no feature
     for (int n = 0; n < n_steps; ++n) {
       const int b = n & 1;
-      const int q0 = (i_start + n) * kBQ;
+      const int q0 = (i_start + n) * kBQ + 32 * half;
       if (!__all_sync(0xffffffffu, mbar_wait(&sh.dq_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status))) break;
       tc_fence_after();
-      uint32_t v[64];
-      if (has_rows) tmem_ld64(tmem_addr(tmem, lane_base, b * kBQ), v);
+      uint32_t v[32];
+      if (has_rows) tmem_ld32(tmem_addr(tmem, lane_base, 128 + b * kBQ + 32 * half), v);
       tc_fence_before();
       mbar_arrive(&sh.dq_empty[b]);
       if (has_rows) {
         float* dst = a.dq + (static_cast<size_t>(bh) * a.N + q0) * D + c;
-        const int rows = min(kBQ, a.N - q0);
+        const int rows = min(32, a.N - q0);
 #pragma unroll
-        for (int q = 0; q < kBQ; ++q)
+        for (int q = 0; q < 32; ++q)
           if (q < rows) atomicAdd(dst + static_cast<size_t>(q) * D, __uint_as_float(v[q]) * a.scale);
       }
     }
