@@ -78,10 +78,6 @@ struct BwdShared {
   int abort;
 };
 
-// Advance a shared-memory descriptor's start address by `bytes` (a multiple of 16
-// that keeps the address inside the same 256 KB window).
-__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
-
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -175,7 +171,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       __syncwarp();
     } else if (warp == kMmaWarp) {
       // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
+      {
+        const uint32_t leader = elect_one() ? 1u : 0u;
         constexpr uint32_t kIdSdP = idesc_bf16_f32(kBKV, kBQ, false, false);  // S^T, dP^T
         constexpr uint32_t kIdKV = idesc_bf16_f32(kBKV, D, false, true);      // dV, dK (A in TMEM)
         constexpr uint32_t kIdQ = idesc_bf16_f32(128, kBQ, true, true);       // dQ^T = K^T dS^T
@@ -189,28 +186,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         const uint64_t dQ_mn = sdesc_sw128(smem_u32(sQ), kBQ * 128, 1024);  // Q stage 0, MN-major (B of dK)
         const uint64_t dDO_mn = sdesc_sw128(smem_u32(sDO), kBQ * 128, 1024);// dO stage 0, MN-major (B of dV)
         const uint64_t dDS_mn = sdesc_sw128(smem_u32(sDS), kBKV * 128, 1024);// dS buffer 0, MN-major (B of dQ^T)
-        bool ok = mbar_wait(&sh.kv_full, 0, &sh.abort, &g_bwd_status);
+        bool ok = warp_wait(&sh.kv_full, 0, &sh.abort, &g_bwd_status);
         // S^T(n) and dP^T(n) into buffer n & 1.  The S^T buffer's previous user (P^T of
         // step n - 2, read by dV) is done by issue order; the dP^T buffer also held
         // dQ^T of step n - 2, so the dQ writers must have drained it first.  S^T goes
         // first so that its products cover that hand-off.
         auto issue_sdp = [&](int n) -> bool {
           const int s = n % C::kStages, b = n & 1;
-          if (!mbar_wait(&sh.q_full[s], (n / C::kStages) & 1, &sh.abort, &g_bwd_status)) return false;
+          if (!warp_wait(&sh.q_full[s], (n / C::kStages) & 1, &sh.abort, &g_bwd_status)) return false;
           tc_fence_after();
           const uint64_t q_d = desc_add(dQ_k, s * C::kQBytes), do_d = desc_add(dDO_k, s * C::kQBytes);
           const uint32_t s_tm = tmem + b * kBQ;
   #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             umma_ss(s_tm, desc_add(dK_k, (kk >> 2) * (kBKV * 128) + (kk & 3) * 32),
-                    desc_add(q_d, (kk >> 2) * (kBQ * 128) + (kk & 3) * 32), kIdSdP, kk > 0);
-          if (n >= 2 && !mbar_wait(&sh.dq_empty[b], ((n >> 1) - 1) & 1, &sh.abort, &g_bwd_status)) return false;
+                    desc_add(q_d, (kk >> 2) * (kBQ * 128) + (kk & 3) * 32), kIdSdP, kk > 0, leader);
+          if (n >= 2 && !warp_wait(&sh.dq_empty[b], ((n >> 1) - 1) & 1, &sh.abort, &g_bwd_status)) return false;
           tc_fence_after();
   #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             umma_ss(s_tm + 128, desc_add(dV_k, (kk >> 2) * (kBKV * 128) + (kk & 3) * 32),
-                    desc_add(do_d, (kk >> 2) * (kBQ * 128) + (kk & 3) * 32), kIdSdP, kk > 0);
-          umma_commit(&sh.sdp_full[b]);
+                    desc_add(do_d, (kk >> 2) * (kBQ * 128) + (kk & 3) * 32), kIdSdP, kk > 0, leader);
+          umma_commit(&sh.sdp_full[b], leader);
           return true;
         };
         if (ok) {
@@ -220,7 +217,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         for (int n = 0; ok && n < n_steps; ++n) {
           const int s = n % C::kStages, b = n & 1;
           if (n + 1 < n_steps && !issue_sdp(n + 1)) break;
-          if (!mbar_wait(&sh.p_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status)) break;
+          if (!warp_wait(&sh.p_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status)) break;
           tc_fence_after();
           const uint64_t q_d = desc_add(dQ_mn, s * C::kQBytes), do_d = desc_add(dDO_mn, s * C::kQBytes);
           const uint32_t s_tm = tmem + b * kBQ;
@@ -228,24 +225,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
           // dV += P^T dO_i   (K = 64 queries; dO_i is the MN-major B operand)
   #pragma unroll
           for (int kk = 0; kk < kBQ / 16; ++kk)
-            umma_ts(tmem + C::kDVCol, s_tm + kk * 8, desc_add(do_d, kk * 16 * 128), kIdKV, kk > 0 ? 1u : acc0);
+            umma_ts(tmem + C::kDVCol, s_tm + kk * 8, desc_add(do_d, kk * 16 * 128), kIdKV, kk > 0 ? 1u : acc0, leader);
           // dK += dS^T Q_i
   #pragma unroll
           for (int kk = 0; kk < kBQ / 16; ++kk)
-            umma_ts(tmem + C::kDKCol, s_tm + 128 + kk * 8, desc_add(q_d, kk * 16 * 128), kIdKV, kk > 0 ? 1u : acc0);
-          umma_commit(&sh.q_empty[s]);
+            umma_ts(tmem + C::kDKCol, s_tm + 128 + kk * 8, desc_add(q_d, kk * 16 * 128), kIdKV, kk > 0 ? 1u : acc0, leader);
+          umma_commit(&sh.q_empty[s], leader);
           // dQ_i^T = K^T dS^T into the dP^T buffer (its dS^T was consumed by the dK MMA above).
           // A = K as an MN-major [d x keys] operand; for d = 64 the upper 64 rows of the
           // M = 128 product read the V tile and are ignored.
           const uint64_t ds_d = desc_add(dDS_mn, b * C::kDSBytes);
   #pragma unroll
           for (int kk = 0; kk < kBKV / 16; ++kk)
-            umma_ss(s_tm + 128, desc_add(dK_mn, kk * 16 * 128), desc_add(ds_d, kk * 16 * 128), kIdQ, kk > 0);
-          umma_commit(&sh.dq_full[b]);
-          umma_commit(&sh.ds_empty[b]);
+            umma_ss(s_tm + 128, desc_add(dK_mn, kk * 16 * 128), desc_add(ds_d, kk * 16 * 128), kIdQ, kk > 0, leader);
+          umma_commit(&sh.dq_full[b], leader);
+          umma_commit(&sh.ds_empty[b], leader);
         }
-        if (ok) umma_commit(&sh.dkdv_full);
-        umma_commit(&sh.drain);
+        if (ok) umma_commit(&sh.dkdv_full, leader);
+        umma_commit(&sh.drain, leader);
         mbar_wait_drain(&sh.drain, 0);
       }
       __syncwarp();

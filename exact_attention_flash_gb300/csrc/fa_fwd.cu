@@ -156,38 +156,42 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       __syncwarp();
     } else if (warp == kMmaWarp) {
       // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
+      {
+        const uint32_t leader = elect_one() ? 1u : 0u;
         constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN, false, false);
         constexpr uint32_t kIdO = idesc_bf16_f32(kBM, D, false, true);
-        const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+        // Descriptors are built once; each MMA only adds a constant offset, which keeps
+        // the single issuing thread's path short (the tensor core's queue is shallow).
+        const uint64_t dQ = sdesc_sw128(smem_u32(sQ), 16, 1024);         // Q tile 0, K-major
+        const uint64_t dK = sdesc_sw128(smem_u32(sK), 16, 1024);         // K stage 0, K-major
+        const uint64_t dV = sdesc_sw128(smem_u32(sV), kBN * 128, 1024);  // V stage 0, MN-major
         auto issue_s = [&](int t, int j) {
           const int s = j % C::kStages;
-          const uint32_t qa = sQa + t * C::kTileBytes, ka = sKa + s * C::kTileBytes;
+          const uint64_t q_d = desc_add(dQ, t * C::kTileBytes), k_d = desc_add(dK, s * C::kTileBytes);
+          const uint32_t s_tm = tmem + t * kBN;
   #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-            umma_ss(tmem_addr(tmem, 0, t * kBN), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                    kIdS, kk > 0);
+            umma_ss(s_tm, desc_add(q_d, off), desc_add(k_d, off), kIdS, kk > 0, leader);
           }
-          umma_commit(&bars.s_full[t]);
+          umma_commit(&bars.s_full[t], leader);
         };
         auto issue_pv = [&](int t, int j) {
           const int s = j % C::kStages;
-          const uint32_t va = sVa + s * C::kTileBytes;
-          const uint32_t o_tm = tmem_addr(tmem, 0, C::kOCol + t * D);
+          const uint64_t v_d = desc_add(dV, s * C::kTileBytes);
+          const uint32_t o_tm = tmem + C::kOCol + t * D, p_tm = tmem + t * kBN;
+          const uint32_t acc0 = j > 0 ? 1u : 0u;
   #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
-            umma_ts(o_tm, tmem_addr(tmem, 0, t * kBN + kk * 8), sdesc_sw128(va + kk * 16 * 128, kBN * 128, 1024), kIdO,
-                    (j > 0 || kk > 0) ? 1u : 0u);
+            umma_ts(o_tm, p_tm + kk * 8, desc_add(v_d, kk * 16 * 128), kIdO, kk > 0 ? 1u : acc0, leader);
           if (kPrecise) {
   #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
-              umma_ts(o_tm, tmem_addr(tmem, 0, t * kBN + 64 + kk * 8), sdesc_sw128(va + kk * 16 * 128, kBN * 128, 1024),
-                      kIdO, 1u);
+              umma_ts(o_tm, p_tm + 64 + kk * 8, desc_add(v_d, kk * 16 * 128), kIdO, 1u, leader);
           }
         };
-        bool ok = mbar_wait(&bars.q_full, 0, &bars.abort, &g_fwd_status) &&
-                  mbar_wait(&bars.k_full[0], 0, &bars.abort, &g_fwd_status);
+        bool ok = warp_wait(&bars.q_full, 0, &bars.abort, &g_fwd_status) &&
+                  warp_wait(&bars.k_full[0], 0, &bars.abort, &g_fwd_status);
         if (ok) {
           tc_fence_after();
           for (int t = 0; t < kTiles; ++t) issue_s(t, 0);
@@ -195,35 +199,35 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         for (int j = 0; ok && j < n_kv_cta; ++j) {
           const int s = j % C::kStages;
           const int jn = j + 1, sn = jn % C::kStages;
-          if (!mbar_wait(&bars.v_full[s], (j / C::kStages) & 1, &bars.abort, &g_fwd_status)) break;
+          if (!warp_wait(&bars.v_full[s], (j / C::kStages) & 1, &bars.abort, &g_fwd_status)) break;
           // tile 0
           if (j < n_kv[0]) {
-            if (!mbar_wait(&bars.p_full[0], j & 1, &bars.abort, &g_fwd_status)) break;
+            if (!warp_wait(&bars.p_full[0], j & 1, &bars.abort, &g_fwd_status)) break;
             tc_fence_after();
             issue_pv(0, j);
             if (jn < n_kv[0]) {
-              if (!mbar_wait(&bars.k_full[sn], (jn / C::kStages) & 1, &bars.abort, &g_fwd_status)) break;
+              if (!warp_wait(&bars.k_full[sn], (jn / C::kStages) & 1, &bars.abort, &g_fwd_status)) break;
               tc_fence_after();
               issue_s(0, jn);
             } else {
-              umma_commit(&bars.o_full[0]);
+              umma_commit(&bars.o_full[0], leader);
             }
           }
           // tile 1
-          if (!mbar_wait(&bars.p_full[1], j & 1, &bars.abort, &g_fwd_status)) break;
+          if (!warp_wait(&bars.p_full[1], j & 1, &bars.abort, &g_fwd_status)) break;
           tc_fence_after();
           issue_pv(1, j);
-          umma_commit(&bars.kv_empty[s]);
+          umma_commit(&bars.kv_empty[s], leader);
           if (jn < n_kv[1]) {
-            if (!mbar_wait(&bars.k_full[sn], (jn / C::kStages) & 1, &bars.abort, &g_fwd_status)) break;
+            if (!warp_wait(&bars.k_full[sn], (jn / C::kStages) & 1, &bars.abort, &g_fwd_status)) break;
             tc_fence_after();
             issue_s(1, jn);
           } else {
-            umma_commit(&bars.o_full[1]);
+            umma_commit(&bars.o_full[1], leader);
           }
         }
         // Drain: all MMAs complete before tensor memory is released.
-        umma_commit(&bars.drain);
+        umma_commit(&bars.drain, leader);
         mbar_wait_drain(&bars.drain, 0);
       }
       __syncwarp();
