@@ -43,6 +43,21 @@ fa_status make_row_tile_map(CUtensorMap* m, const void* ptr, int BH, int N, int 
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// dQ [B*H, N, d] fp32 as a 3-D tensor, tiles of 64 rows x d features (no swizzle):
+// the target of the backward's bulk fp32 reductions; rows past N are dropped.
+fa_status make_dq_reduce_map(CUtensorMap* m, void* ptr, int BH, int N, int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return FA_ERR_CUDA;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(d), 64, 1};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, elem,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 fa_status check_common(int B, int H, int N, int d) {
@@ -127,6 +142,7 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   if ((st = make_row_tile_map(&a.tm_k, k, BH, N, d, 128)) != FA_OK) return st;
   if ((st = make_row_tile_map(&a.tm_v, v, BH, N, d, 128)) != FA_OK) return st;
   if ((st = make_row_tile_map(&a.tm_do, dout, BH, N, d, 64)) != FA_OK) return st;
+  if ((st = make_dq_reduce_map(&a.tm_dq, dq, BH, N, d)) != FA_OK) return st;
   a.o = o;
   a.dout = dout;
   a.lse = lse;

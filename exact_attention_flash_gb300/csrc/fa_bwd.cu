@@ -64,8 +64,9 @@ struct BwdCfg {
   static constexpr int kDVCol = 256;
   static constexpr int kDKCol = 256 + D;
   static constexpr int kRowBytes = kBQ * 4;      // one step's -LSE*log2(e) (or -D) slice
+  static constexpr int kDQBytes = kBQ * D * 4;   // fp32 dQ tile staged for the bulk reduction
   static constexpr int kSmemBytes =
-      2 * kKVBytes + kStages * 2 * kQBytes + 2 * kDSBytes + kStages * 2 * kRowBytes + 1024;
+      2 * kKVBytes + kStages * 2 * kQBytes + 2 * kDSBytes + kDQBytes + kStages * 2 * kRowBytes + 1024;
 };
 
 struct BwdShared {
@@ -82,6 +83,32 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Named barrier over the 256 dQ-writer threads.
+__device__ __forceinline__ void writer_bar_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// The same barrier, also AND-ing a flag across the writers, so that after a failed
+// wait every writer thread takes the same path.
+__device__ __forceinline__ bool writer_bar_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n barrier.cta.red.and.pred p, 1, 256, q;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
+
+// dQ[bh, q0 : q0 + 64, :] += staged tile (fp32 add performed in L2; rows past N are dropped).
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_constant__ BackwardArgs a) {
   using C = BwdCfg<D>;
@@ -92,7 +119,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
   uint8_t* sQ = sV + C::kKVBytes;                       // [kStages][kQBytes]
   uint8_t* sDO = sQ + C::kStages * C::kQBytes;          // [kStages][kQBytes]
   uint8_t* sDS = sDO + C::kStages * C::kQBytes;         // [2][kDSBytes]
-  float* sNL = reinterpret_cast<float*>(sDS + 2 * C::kDSBytes);  // [kStages][kBQ] -LSE*log2(e)
+  float* sDQ = reinterpret_cast<float*>(sDS + 2 * C::kDSBytes);  // [kBQ][D] fp32 dQ staging tile
+  float* sNL = sDQ + kBQ * D;                                     // [kStages][kBQ] -LSE*log2(e)
   float* sND = sNL + C::kStages * kBQ;                            // [kStages][kBQ] -D
   __shared__ BwdShared sh;
 
@@ -338,29 +366,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kWriterRegs));
     // ------------------------------------------------------------ dQ writers (thread = feature)
     // dQ_i^T sits in TMEM with one feature per lane and one query per column.  Each
-    // writer warpgroup takes 32 of the 64 query columns and adds them into dQ with
-    // fp32 reductions in L2 (a warp's 32 lanes cover 128 contiguous bytes of a row).
+    // writer warpgroup takes 32 of the 64 query columns, transposes them into a
+    // [64 x d] fp32 tile in shared memory, and one thread adds the whole tile into dQ
+    // with a single TMA bulk reduction (the fp32 adds happen in L2).  The tile is
+    // rewritten only after the previous reduction has finished reading it.
     const int half = (warp - kWriterWarp0) >> 2;  // query columns [32*half, 32*half + 32)
     const int lane_base = (warp & 3) * 32;
     const int c = lane_base + lane;               // feature index == TMEM lane of dQ^T
     const bool has_rows = lane_base < D;          // for d = 64, lanes 64..127 hold no feature
+    const bool leader = (tid == kWriterWarp0 * 32);
     for (int n = 0; n < n_steps; ++n) {
       const int b = n & 1;
-      const int q0 = (i_start + n) * kBQ + 32 * half;
-      if (!__all_sync(0xffffffffu, mbar_wait(&sh.dq_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status))) break;
-      tc_fence_after();
+      const int q0 = (i_start + n) * kBQ;
+      const bool w_ok = __all_sync(0xffffffffu, mbar_wait(&sh.dq_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status));
       uint32_t v[32];
-      if (has_rows) tmem_ld32(tmem_addr(tmem, lane_base, 128 + b * kBQ + 32 * half), v);
-      tc_fence_before();
-      mbar_arrive(&sh.dq_empty[b]);
-      if (has_rows) {
-        float* dst = a.dq + (static_cast<size_t>(bh) * a.N + q0) * D + c;
-        const int rows = min(32, a.N - q0);
-#pragma unroll
-        for (int q = 0; q < 32; ++q)
-          if (q < rows) atomicAdd(dst + static_cast<size_t>(q) * D, __uint_as_float(v[q]) * a.scale);
+      if (w_ok) {
+        tc_fence_after();
+        if (has_rows) tmem_ld32(tmem_addr(tmem, lane_base, 128 + b * kBQ + 32 * half), v);
+        tc_fence_before();
+        mbar_arrive(&sh.dq_empty[b]);
       }
+      if (leader && n > 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      if (!writer_bar_and(w_ok)) break;  // staging tile free; all writers go on or all stop
+      if (has_rows) {
+#pragma unroll
+        for (int q = 0; q < 32; ++q) sDQ[(32 * half + q) * D + c] = __uint_as_float(v[q]) * a.scale;
+      }
+      fence_proxy_async_smem();
+      writer_bar_sync();  // tile complete
+      if (leader) tma_reduce_add_3d(&a.tm_dq, sDQ, 0, q0, bh);
     }
+    if (leader) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
 
   tc_fence_before();
