@@ -64,7 +64,7 @@ struct FwdCfg {
 struct FwdBarriers {
   uint64_t q_full;
   uint64_t k_full[4], v_full[4], kv_empty[4];
-  uint64_t s_full[kTiles], p_full[kTiles], o_full[kTiles];
+  uint64_t s_full[kTiles], p_half[kTiles], p_full[kTiles], o_full[kTiles];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     }
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(&bars.s_full[t], 1);
+      mbar_init(&bars.p_half[t], kBM);
       mbar_init(&bars.p_full[t], kBM);
       mbar_init(&bars.o_full[t], 1);
     }
@@ -176,19 +177,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           }
           umma_commit(&bars.s_full[t], leader);
         };
-        auto issue_pv = [&](int t, int j) {
+        // O_t += P_t V_j in two halves of 64 keys: the softmax releases P's first
+        // half (p_half) while it still computes the second (p_full).
+        auto issue_pv = [&](int t, int j) -> bool {
           const int s = j % C::kStages;
           const uint64_t v_d = desc_add(dV, s * C::kTileBytes);
           const uint32_t o_tm = tmem + C::kOCol + t * D, p_tm = tmem + t * kBN;
           const uint32_t acc0 = j > 0 ? 1u : 0u;
+          if (!warp_wait(&bars.p_half[t], j & 1, &bars.abort, &g_fwd_status)) return false;
+          tc_fence_after();
   #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
+          for (int kk = 0; kk < kBN / 32; ++kk)
             umma_ts(o_tm, p_tm + kk * 8, desc_add(v_d, kk * 16 * 128), kIdO, kk > 0 ? 1u : acc0, leader);
+          if (!warp_wait(&bars.p_full[t], j & 1, &bars.abort, &g_fwd_status)) return false;
+          tc_fence_after();
+  #pragma unroll
+          for (int kk = kBN / 32; kk < kBN / 16; ++kk)
+            umma_ts(o_tm, p_tm + kk * 8, desc_add(v_d, kk * 16 * 128), kIdO, 1u, leader);
           if (kPrecise) {
   #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
               umma_ts(o_tm, p_tm + 64 + kk * 8, desc_add(v_d, kk * 16 * 128), kIdO, 1u, leader);
           }
+          return true;
         };
         bool ok = warp_wait(&bars.q_full, 0, &bars.abort, &g_fwd_status) &&
                   warp_wait(&bars.k_full[0], 0, &bars.abort, &g_fwd_status);
@@ -202,9 +213,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           if (!warp_wait(&bars.v_full[s], (j / C::kStages) & 1, &bars.abort, &g_fwd_status)) break;
           // tile 0
           if (j < n_kv[0]) {
-            if (!warp_wait(&bars.p_full[0], j & 1, &bars.abort, &g_fwd_status)) break;
-            tc_fence_after();
-            issue_pv(0, j);
+            if (!issue_pv(0, j)) break;
             if (jn < n_kv[0]) {
               if (!warp_wait(&bars.k_full[sn], (jn / C::kStages) & 1, &bars.abort, &g_fwd_status)) break;
               tc_fence_after();
@@ -214,9 +223,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             }
           }
           // tile 1
-          if (!warp_wait(&bars.p_full[1], j & 1, &bars.abort, &g_fwd_status)) break;
-          tc_fence_after();
-          issue_pv(1, j);
+          if (!issue_pv(1, j)) break;
           umma_commit(&bars.kv_empty[s], leader);
           if (jn < n_kv[1]) {
             if (!warp_wait(&bars.k_full[sn], (jn / C::kStages) & 1, &bars.abort, &g_fwd_status)) break;
@@ -320,6 +327,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           }
         }
         tmem_st32(s_tm + half * 32, u);
+        if (!kPrecise && half == 0) {  // keys 0..63 are ready for the PV product
+          tc_fence_before();
+          mbar_arrive(&bars.p_half[t]);
+        }
       }
       if (kPrecise) {  // residuals over columns 64..127 (the S values there are consumed)
 #pragma unroll
@@ -350,6 +361,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       l_hat = kPrecise ? l_run : l_hat * alpha + (rowsum + delta_max);
       m_run = m_use;
       tc_fence_before();
+      if (kPrecise) mbar_arrive(&bars.p_half[t]);
       mbar_arrive(&bars.p_full[t]);
     }
     // ------------------------------------------------------------ epilogue
