@@ -19,7 +19,7 @@
 //   warps 0-3   softmax for tile 0, warps 4-7 for tile 1: thread r owns query
 //               row r (TMEM lane r), loads its row of S, takes the row max in
 //               registers, writes P as bf16 over the S columns, and rescales its
-//               row of O in TMEM when the running max grows by more than 2^8
+//               row of O in TMEM when the running max grows by more than a factor 2^32
 //               (the final O / l uses the same reference max, so this is exact).
 // Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 and O_1 after.
 // Work is done in base 2: x = S * scale * log2(e), p = 2^(x - m).
@@ -49,7 +49,14 @@ constexpr int kFwdThreads = 384;  // warps 10-11 only lend their registers to th
 constexpr int kSoftmaxRegs = 216;
 constexpr int kOtherRegs = 64;
 constexpr int kRegsNeeded = 256 * kSoftmaxRegs + 128 * kOtherRegs;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Lazy rescaling: the reference max m of a row moves (and O is rescaled) only when
+// a tile's max exceeds it by more than this many log2 units, so the weights
+// 2^(s - m) stay below 2^32.  fp32 and bf16 share one exponent range: the sum of N
+// weights stays below 2^(32 + log2 N) and O below that times max|v|, inside fp32
+// for N < 2^31 and |v| < 2^64.  Rounding of P to bf16 is relative, so the
+// threshold does not change the error of O; it only makes rescales rare when the
+// row max keeps rising (large logits).
+constexpr float kRescaleThreshold = 32.0f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D>
@@ -346,7 +353,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       const float rowsum = s4.x + s4.y;
       // Normaliser of O.  P enters the PV product rounded to bf16.  With the
       // reference max held back (lazy rescaling) the row's largest weight is
-      // 2^(x_max - m) <= 2^8 instead of exactly 1, and its rounding error would
+      // 2^(x_max - m) <= 2^32 instead of exactly 1, and its rounding error would
       // bias O by up to 2^-9 of a V row.  Adding that one element's rounding
       // error to the exact sum removes the bias; the other weights' rounding
       // errors are bounded and unbiased as in the standard bf16-P scheme.
