@@ -47,7 +47,7 @@ constexpr int kFwdThreads = 384;  // warps 10-11 only lend their registers to th
 // (producer, MMA issuer, two idle warps) lowers it.  The sum must stay within what
 // the CTA was launched with; the launcher checks this against the compiled kernel.
 constexpr int kSoftmaxRegs = 216;
-constexpr int kOtherRegs = 64;
+constexpr int kOtherRegs = 72;
 constexpr int kRegsNeeded = 256 * kSoftmaxRegs + 128 * kOtherRegs;
 // Lazy rescaling: the reference max m of a row moves (and O is rescaled) only when
 // a tile's max exceeds it by more than this many log2 units, so the weights
