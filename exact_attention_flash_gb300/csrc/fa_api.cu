@@ -43,20 +43,6 @@ fa_status make_row_tile_map(CUtensorMap* m, const void* ptr, int BH, int N, int 
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-// dQ [B*H, N, d] fp32 as a 3-D tensor, tiles of 64 rows x d features (no swizzle):
-// the target of the backward's bulk fp32 reductions; rows past N are dropped.
-fa_status make_dq_reduce_map(CUtensorMap* m, void* ptr, int BH, int N, int d) {
-  EncodeTiledFn enc = encode_fn();
-  if (enc == nullptr) return FA_ERR_CUDA;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(d), 64, 1};
-  const cuuint32_t elem[3] = {1, 1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, elem,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
-}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -116,12 +102,13 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, fa_dt
   return fa::launch_forward(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-// Two fp32 arrays over [B*H, N rounded up to 64]: -LSE*log2(e) and -D per query row.
+// Per query row over [B*H, N rounded up to 64]: two 32-byte rows of the bias tiles
+// (-LSE/scale and -D as three bf16 terms each).
 size_t fa_backward_workspace_size(int B, int H, int N, int d) {
   (void)d;
   if (B < 1 || H < 1 || N < 1) return 0;
   const size_t n_pad = round_up(static_cast<size_t>(N), 64);
-  return 2 * round_up(static_cast<size_t>(B) * H * n_pad * sizeof(float), 256);
+  return static_cast<size_t>(B) * H * n_pad * 64;
 }
 
 fa_status fa_backward(const void* q, const void* k, const void* v, const void* o, fa_dtype o_dtype,
@@ -142,7 +129,6 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   if ((st = make_row_tile_map(&a.tm_k, k, BH, N, d, 128)) != FA_OK) return st;
   if ((st = make_row_tile_map(&a.tm_v, v, BH, N, d, 128)) != FA_OK) return st;
   if ((st = make_row_tile_map(&a.tm_do, dout, BH, N, d, 64)) != FA_OK) return st;
-  if ((st = make_dq_reduce_map(&a.tm_dq, dq, BH, N, d)) != FA_OK) return st;
   a.o = o;
   a.dout = dout;
   a.lse = lse;
@@ -150,9 +136,7 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   a.dk = dk;
   a.dv = dv;
   a.n_pad = static_cast<int>(round_up(static_cast<size_t>(N), 64));
-  a.neg_lse2 = static_cast<float*>(workspace);
-  a.neg_delta = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                         round_up(static_cast<size_t>(B) * H * a.n_pad * sizeof(float), 256));
+  a.bias = static_cast<uint8_t*>(workspace);
   a.B = B;
   a.H = H;
   a.N = N;

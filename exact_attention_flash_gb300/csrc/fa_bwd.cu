@@ -39,21 +39,20 @@ __device__ unsigned g_bwd_status;
 
 constexpr int kBKV = 128;  // keys per CTA
 constexpr int kBQ = 64;    // queries per step
-// Warps 0-3: P^T / dS^T; warps 4-11: dQ writers (two warpgroups, one per half of
-// the step's 64 query columns); warp 12: TMA producer; warp 13: MMA issuer;
-// warps 14-15 only lend their registers.
-constexpr int kBwdThreads = 512;
-constexpr int kWriterWarp0 = 4;
-constexpr int kProducerWarp = 12;
-constexpr int kMmaWarp = 13;
-// Register split (setmaxnreg) by warpgroup: P/dS warps hold two 64-column TMEM
-// rows in registers, each dQ writer one 32-column row, the producer / MMA warps
-// little.  The sum stays within the CTA's launch allocation; the launcher checks it.
-constexpr int kComputeRegs = 232;
-constexpr int kWriterRegs = 64;
-constexpr int kOtherRegs = 88;
-constexpr int kRegsNeeded = 128 * kComputeRegs + 256 * kWriterRegs + 128 * kOtherRegs;
-constexpr float kLog2e = 1.4426950408889634f;
+// Warps 0-7: P^T / dS^T and warps 8-15: dQ writers (each two warpgroups, one per
+// half of the step's 64 query columns); warp 16: TMA producer; warp 17: MMA
+// issuer; warps 18-19 only lend their registers.
+constexpr int kBwdThreads = 640;
+constexpr int kWriterWarp0 = 8;
+constexpr int kProducerWarp = 16;
+constexpr int kMmaWarp = 17;
+// Register split (setmaxnreg) by warpgroup: each P/dS thread holds two 32-column
+// TMEM rows, each dQ writer one 32-column row, the producer / MMA warps little.
+// The sum stays within the CTA's launch allocation; the launcher checks it.
+constexpr int kComputeRegs = 120;
+constexpr int kWriterRegs = 72;
+constexpr int kOtherRegs = 96;
+constexpr int kRegsNeeded = 256 * kComputeRegs + 256 * kWriterRegs + 128 * kOtherRegs;
 
 template <int D>
 struct BwdCfg {
@@ -63,10 +62,13 @@ struct BwdCfg {
   static constexpr int kDSBytes = kBKV * kBQ * 2; // dS tile (bf16), 16 KB
   static constexpr int kDVCol = 256;
   static constexpr int kDKCol = 256 + D;
-  static constexpr int kRowBytes = kBQ * 4;      // one step's -LSE*log2(e) (or -D) slice
-  static constexpr int kDQBytes = kBQ * D * 4;   // fp32 dQ tile staged for the bulk reduction
+  // Per step: the two bias tiles (B operands, 64 queries x 16, bf16): -LSE/scale
+  // and -D, each split into three bf16 terms.  Their A operand is a constant
+  // 128 x 16 tile with ones in columns 0-2.
+  static constexpr int kBiasBytes = 2 * kBQ * 16 * 2;
+  static constexpr int kOnesBytes = kBKV * 16 * 2;
   static constexpr int kSmemBytes =
-      2 * kKVBytes + kStages * 2 * kQBytes + 2 * kDSBytes + kDQBytes + kStages * 2 * kRowBytes + 1024;
+      2 * kKVBytes + kStages * 2 * kQBytes + 2 * kDSBytes + kStages * kBiasBytes + kOnesBytes + 1024;
 };
 
 struct BwdShared {
@@ -83,32 +85,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Named barrier over the 256 dQ-writer threads.
-__device__ __forceinline__ void writer_bar_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
-// The same barrier, also AND-ing a flag across the writers, so that after a failed
-// wait every writer thread takes the same path.
-__device__ __forceinline__ bool writer_bar_and(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n barrier.cta.red.and.pred p, 1, 256, q;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(v))
-      : "memory");
-  return r != 0;
-}
-
-// dQ[bh, q0 : q0 + 64, :] += staged tile (fp32 add performed in L2; rows past N are dropped).
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_constant__ BackwardArgs a) {
   using C = BwdCfg<D>;
@@ -119,9 +95,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
   uint8_t* sQ = sV + C::kKVBytes;                       // [kStages][kQBytes]
   uint8_t* sDO = sQ + C::kStages * C::kQBytes;          // [kStages][kQBytes]
   uint8_t* sDS = sDO + C::kStages * C::kQBytes;         // [2][kDSBytes]
-  float* sDQ = reinterpret_cast<float*>(sDS + 2 * C::kDSBytes);  // [kBQ][D] fp32 dQ staging tile
-  float* sNL = sDQ + kBQ * D;                                     // [kStages][kBQ] -LSE*log2(e)
-  float* sND = sNL + C::kStages * kBQ;                            // [kStages][kBQ] -D
+  uint8_t* sBias = sDS + 2 * C::kDSBytes;               // [kStages][kBiasBytes]
+  uint8_t* sOnes = sBias + C::kStages * C::kBiasBytes;  // [kOnesBytes]
   __shared__ BwdShared sh;
 
   const int tid = threadIdx.x;
@@ -145,7 +120,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.sdp_full[b], 1);
-      mbar_init(&sh.p_full[b], 128);
+      mbar_init(&sh.p_full[b], 256);
       mbar_init(&sh.dq_full[b], 1);
       mbar_init(&sh.dq_empty[b], 256);
       mbar_init(&sh.ds_empty[b], 1);
@@ -154,6 +129,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     mbar_init(&sh.drain, 1);
     fence_barrier_init();
   }
+  // The ones tile, in the no-swizzle K-major layout of 8-row x 16-byte core matrices:
+  // even core matrices hold columns 0-7 (1, 1, 1, 0, ...), odd ones columns 8-15 (0).
+  for (int i = tid; i < C::kOnesBytes / 16; i += kBwdThreads)
+    reinterpret_cast<uint4*>(sOnes)[i] = ((i >> 3) & 1) ? make_uint4(0u, 0u, 0u, 0u) : make_uint4(0x3F803F80u, 0x3F80u, 0u, 0u);
+  fence_proxy_async_smem();
   if (warp == 0) tmem_alloc(&sh.tmem_base, 512);
   tc_fence_before();
   __syncthreads();
@@ -181,15 +161,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
           if (n >= C::kStages && !mbar_wait(&sh.q_empty[s], ((n / C::kStages) - 1) & 1, &sh.abort, &g_bwd_status))
             break;
           const int q0 = (i_start + n) * kBQ;
-          mbar_arrive_expect_tx(&sh.q_full[s], 2 * C::kQBytes + 2 * C::kRowBytes);
+          mbar_arrive_expect_tx(&sh.q_full[s], 2 * C::kQBytes + C::kBiasBytes);
           for (int c = 0; c < D / 64; ++c) {
             tma_load_3d(sQ + s * C::kQBytes + c * (kBQ * 128), &a.tm_q, &sh.q_full[s], c * 64, q0, bh);
             tma_load_3d(sDO + s * C::kQBytes + c * (kBQ * 128), &a.tm_do, &sh.q_full[s], c * 64, q0, bh);
           }
-          // Row slices of the padded [B*H, n_pad] workspace arrays (always in bounds, 256-byte aligned).
-          const size_t row_off = static_cast<size_t>(bh) * a.n_pad + q0;
-          bulk_load(sNL + s * kBQ, a.neg_lse2 + row_off, C::kRowBytes, &sh.q_full[s]);
-          bulk_load(sND + s * kBQ, a.neg_delta + row_off, C::kRowBytes, &sh.q_full[s]);
+          // The query block's bias tiles from the workspace (always in bounds, 4 KB aligned).
+          const size_t blk = static_cast<size_t>(bh) * (a.n_pad / kBQ) + (i_start + n);
+          bulk_load(sBias + s * C::kBiasBytes, a.bias + blk * C::kBiasBytes, C::kBiasBytes, &sh.q_full[s]);
           ++issued;
         }
         mbar_wait_drain(&sh.kv_full, 0);
@@ -214,27 +193,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         const uint64_t dQ_mn = sdesc_sw128(smem_u32(sQ), kBQ * 128, 1024);  // Q stage 0, MN-major (B of dK)
         const uint64_t dDO_mn = sdesc_sw128(smem_u32(sDO), kBQ * 128, 1024);// dO stage 0, MN-major (B of dV)
         const uint64_t dDS_mn = sdesc_sw128(smem_u32(sDS), kBKV * 128, 1024);// dS buffer 0, MN-major (B of dQ^T)
+        const uint64_t dOnes = sdesc_k16_noswizzle(smem_u32(sOnes));        // A of the bias products
+        const uint64_t dBias = sdesc_k16_noswizzle(smem_u32(sBias));        // bias tiles, stage 0
         bool ok = warp_wait(&sh.kv_full, 0, &sh.abort, &g_bwd_status);
         // S^T(n) and dP^T(n) into buffer n & 1.  The S^T buffer's previous user (P^T of
         // step n - 2, read by dV) is done by issue order; the dP^T buffer also held
         // dQ^T of step n - 2, so the dQ writers must have drained it first.  S^T goes
-        // first so that its products cover that hand-off.
+        // first so that its products cover that hand-off.  Each accumulator starts
+        // from its bias (one K = 16 product: ones x the three bf16 terms), so it ends
+        // holding S^T - LSE/scale and dP^T - D.
         auto issue_sdp = [&](int n) -> bool {
           const int s = n % C::kStages, b = n & 1;
           if (!warp_wait(&sh.q_full[s], (n / C::kStages) & 1, &sh.abort, &g_bwd_status)) return false;
           tc_fence_after();
           const uint64_t q_d = desc_add(dQ_k, s * C::kQBytes), do_d = desc_add(dDO_k, s * C::kQBytes);
           const uint32_t s_tm = tmem + b * kBQ;
+          const uint64_t bias_d = desc_add(dBias, s * C::kBiasBytes);
+          umma_ss(s_tm, dOnes, bias_d, kIdSdP, 0u, leader);
   #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             umma_ss(s_tm, desc_add(dK_k, (kk >> 2) * (kBKV * 128) + (kk & 3) * 32),
-                    desc_add(q_d, (kk >> 2) * (kBQ * 128) + (kk & 3) * 32), kIdSdP, kk > 0, leader);
+                    desc_add(q_d, (kk >> 2) * (kBQ * 128) + (kk & 3) * 32), kIdSdP, 1u, leader);
           if (n >= 2 && !warp_wait(&sh.dq_empty[b], ((n >> 1) - 1) & 1, &sh.abort, &g_bwd_status)) return false;
           tc_fence_after();
+          umma_ss(s_tm + 128, dOnes, desc_add(bias_d, C::kBiasBytes / 2), kIdSdP, 0u, leader);
   #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             umma_ss(s_tm + 128, desc_add(dV_k, (kk >> 2) * (kBKV * 128) + (kk & 3) * 32),
-                    desc_add(do_d, (kk >> 2) * (kBQ * 128) + (kk & 3) * 32), kIdSdP, kk > 0, leader);
+                    desc_add(do_d, (kk >> 2) * (kBQ * 128) + (kk & 3) * 32), kIdSdP, 1u, leader);
           umma_commit(&sh.sdp_full[b], leader);
           return true;
         };
@@ -250,14 +236,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
           const uint64_t q_d = desc_add(dQ_mn, s * C::kQBytes), do_d = desc_add(dDO_mn, s * C::kQBytes);
           const uint32_t s_tm = tmem + b * kBQ;
           const uint32_t acc0 = n > 0 ? 1u : 0u;
-          // dV += P^T dO_i   (K = 64 queries; dO_i is the MN-major B operand)
+          // dV += P^T dO_i   (K = 64 queries; dO_i is the MN-major B operand).  P^T of
+          // query half h sits packed in columns [32h, 32h + 16) of the S^T buffer,
+          // dS^T likewise in the dP^T buffer.
+          auto pcol = [](int kk) { return (kk >> 1) * 32 + (kk & 1) * 8; };
   #pragma unroll
           for (int kk = 0; kk < kBQ / 16; ++kk)
-            umma_ts(tmem + C::kDVCol, s_tm + kk * 8, desc_add(do_d, kk * 16 * 128), kIdKV, kk > 0 ? 1u : acc0, leader);
+            umma_ts(tmem + C::kDVCol, s_tm + pcol(kk), desc_add(do_d, kk * 16 * 128), kIdKV, kk > 0 ? 1u : acc0, leader);
           // dK += dS^T Q_i
   #pragma unroll
           for (int kk = 0; kk < kBQ / 16; ++kk)
-            umma_ts(tmem + C::kDKCol, s_tm + 128 + kk * 8, desc_add(q_d, kk * 16 * 128), kIdKV, kk > 0 ? 1u : acc0, leader);
+            umma_ts(tmem + C::kDKCol, s_tm + 128 + pcol(kk), desc_add(q_d, kk * 16 * 128), kIdKV, kk > 0 ? 1u : acc0, leader);
           umma_commit(&sh.q_empty[s], leader);
           // dQ_i^T = K^T dS^T into the dP^T buffer (its dS^T was consumed by the dK MMA above).
           // A = K as an MN-major [d x keys] operand; for d = 64 the upper 64 rows of the
@@ -275,18 +264,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       }
       __syncwarp();
     }
-  } else if (warp < 4) {
+  } else if (warp < kWriterWarp0) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kComputeRegs));
     // ------------------------------------------------------------ P^T and dS^T (thread = key)
-    const int k = tid;
+    // Warpgroup h takes query columns [32h, 32h + 32) of each step; each element is
+    // independent, so the two warpgroups never exchange data.
+    const int k = tid & (kBKV - 1);
+    const int h = warp >> 2;
     const int key = key0 + k;
-    const int lane_base = warp * 32;
+    const int lane_base = (warp & 3) * 32;
     const float sl2 = a.scale_log2;
     bool ok = true;
     for (int n = 0; n < n_steps; ++n) {
       const int b = n & 1;
       const int q0 = (i_start + n) * kBQ;
-      const int st = n % C::kStages;  // Q/dO stage of this step: holds its -LSE*log2(e) and -D
       if (!__all_sync(0xffffffffu, mbar_wait(&sh.sdp_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status))) {
         ok = false;
         break;
@@ -299,43 +290,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       const bool need_mask = (a.causal && key0 + kBKV - 1 > q0) || (key0 + kBKV > a.N);
       const int first_visible_q = a.causal ? key : 0;  // queries before this key see nothing of it
       const bool key_valid = key < a.N;
-      const uint32_t s_tm = tmem_addr(tmem, lane_base, b * kBQ);
-      const uint32_t dp_tm = tmem_addr(tmem, lane_base, 128 + b * kBQ);
+      const uint32_t s_tm = tmem_addr(tmem, lane_base, b * kBQ + 32 * h);
+      const uint32_t dp_tm = tmem_addr(tmem, lane_base, 128 + b * kBQ + 32 * h);
       uint8_t* ds_row = sDS + b * C::kDSBytes + (k >> 3) * 1024 + (k & 7) * 128;
-      // One TMEM round trip in (S^T and dP^T, 64 columns each) and one out.
-      uint32_t sv[64], dpv[64];
-      tmem_ld64x2(s_tm, dp_tm, sv, dpv);
-      uint32_t pk[32], dk[32];
+      // One TMEM round trip in (S^T and dP^T, 32 columns each) and one out.
+      uint32_t sv[32], dpv[32];
+      tmem_ld32x2(s_tm, dp_tm, sv, dpv);
+      uint32_t pk[16], dk[16];
       const float2 sl2x2 = make_float2(sl2, sl2);
+      // sv holds S^T - LSE/scale, dpv holds dP^T - D (the biases came with the products).
 #pragma unroll
-      for (int e4 = 0; e4 < kBQ; e4 += 4) {
-        const float4 nl = *reinterpret_cast<const float4*>(sNL + st * kBQ + e4);
-        const float4 nd = *reinterpret_cast<const float4*>(sND + st * kBQ + e4);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int e = e4 + 2 * h;
-          const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2x2,
-                                        h == 0 ? make_float2(nl.x, nl.y) : make_float2(nl.z, nl.w));
-          float p0 = ex2(arg.x), p1 = ex2(arg.y);
-          if (need_mask) {
-            if (!key_valid || q0 + e < first_visible_q) p0 = 0.f;
-            if (!key_valid || q0 + e + 1 < first_visible_q) p1 = 0.f;
-          }
-          const float2 ds2 =
-              __fmul2_rn(make_float2(p0, p1),
-                         __fadd2_rn(make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])),
-                                    h == 0 ? make_float2(nd.x, nd.y) : make_float2(nd.z, nd.w)));
-          pk[e / 2] = pack_bf16(p0, p1);
-          dk[e / 2] = pack_bf16(ds2.x, ds2.y);
+      for (int e = 0; e < 32; e += 2) {
+        const float2 arg = __fmul2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2x2);
+        float p0 = ex2(arg.x), p1 = ex2(arg.y);
+        if (need_mask) {
+          const int qe = q0 + 32 * h + e;
+          if (!key_valid || qe < first_visible_q) p0 = 0.f;
+          if (!key_valid || qe + 1 < first_visible_q) p1 = 0.f;
         }
+        const float2 ds2 =
+            __fmul2_rn(make_float2(p0, p1), make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])));
+        pk[e / 2] = pack_bf16(p0, p1);
+        dk[e / 2] = pack_bf16(ds2.x, ds2.y);
       }
       // dS^T row of this key into the MN-major, 128B-swizzled dS tile:
       // 16-byte piece p (queries 8p..8p+7) of row k sits at ((p ^ (k & 7)) * 16).
 #pragma unroll
-      for (int piece = 0; piece < 8; ++piece)
-        *reinterpret_cast<uint4*>(ds_row + ((piece ^ (k & 7)) << 4)) =
+      for (int piece = 0; piece < 4; ++piece)
+        *reinterpret_cast<uint4*>(ds_row + (((4 * h + piece) ^ (k & 7)) << 4)) =
             make_uint4(dk[4 * piece], dk[4 * piece + 1], dk[4 * piece + 2], dk[4 * piece + 3]);
-      tmem_st32x2(s_tm, pk, dp_tm, dk);
+      // P^T and dS^T packed (queries 2c, 2c+1 in column c) over the first 16 of this
+      // half's 32 columns, which this thread has already read.
+      tmem_st16x2(s_tm, pk, dp_tm, dk);
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(&sh.p_full[b]);
@@ -344,8 +330,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     if (ok && __all_sync(0xffffffffu, mbar_wait(&sh.dkdv_full, 0, &sh.abort, &g_bwd_status))) {
       tc_fence_after();
       const size_t row_off = (static_cast<size_t>(bh) * a.N + key) * D;
+      // Warpgroup h stores feature columns [h d/2, (h + 1) d/2) of dK and dV.
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
+      for (int c = h * (D / 2); c < (h + 1) * (D / 2); c += 32) {
         uint32_t uv[32], uk[32];
         tmem_ld32(tmem_addr(tmem, lane_base, C::kDVCol + c), uv);
         tmem_ld32(tmem_addr(tmem, lane_base, C::kDKCol + c), uk);
@@ -366,37 +353,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kWriterRegs));
     // ------------------------------------------------------------ dQ writers (thread = feature)
     // dQ_i^T sits in TMEM with one feature per lane and one query per column.  Each
-    // writer warpgroup takes 32 of the 64 query columns, transposes them into a
-    // [64 x d] fp32 tile in shared memory, and one thread adds the whole tile into dQ
-    // with a single TMA bulk reduction (the fp32 adds happen in L2).  The tile is
-    // rewritten only after the previous reduction has finished reading it.
+    // writer warpgroup takes 32 of the 64 query columns and adds them into dQ with
+    // fp32 reductions in L2, straight from registers: for each query, a warp's 32
+    // lanes cover 128 contiguous bytes of the dQ row.
     const int half = (warp - kWriterWarp0) >> 2;  // query columns [32*half, 32*half + 32)
     const int lane_base = (warp & 3) * 32;
     const int c = lane_base + lane;               // feature index == TMEM lane of dQ^T
     const bool has_rows = lane_base < D;          // for d = 64, lanes 64..127 hold no feature
-    const bool leader = (tid == kWriterWarp0 * 32);
     for (int n = 0; n < n_steps; ++n) {
       const int b = n & 1;
-      const int q0 = (i_start + n) * kBQ;
-      const bool w_ok = __all_sync(0xffffffffu, mbar_wait(&sh.dq_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status));
+      const int q0 = (i_start + n) * kBQ + 32 * half;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sh.dq_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status))) break;
       uint32_t v[32];
-      if (w_ok) {
-        tc_fence_after();
-        if (has_rows) tmem_ld32(tmem_addr(tmem, lane_base, 128 + b * kBQ + 32 * half), v);
-        tc_fence_before();
-        mbar_arrive(&sh.dq_empty[b]);
-      }
-      if (leader && n > 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-      if (!writer_bar_and(w_ok)) break;  // staging tile free; all writers go on or all stop
+      tc_fence_after();
+      if (has_rows) tmem_ld32(tmem_addr(tmem, lane_base, 128 + b * kBQ + 32 * half), v);
+      tc_fence_before();
+      mbar_arrive(&sh.dq_empty[b]);
       if (has_rows) {
+        float* dst = a.dq + (static_cast<size_t>(bh) * a.N + q0) * D + c;
+        const int rows = min(32, a.N - q0);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) sDQ[(32 * half + q) * D + c] = __uint_as_float(v[q]) * a.scale;
+        for (int q = 0; q < 32; ++q)
+          if (q < rows) atomicAdd(dst + static_cast<size_t>(q) * D, __uint_as_float(v[q]) * a.scale);
       }
-      fence_proxy_async_smem();
-      writer_bar_sync();  // tile complete
-      if (leader) tma_reduce_add_3d(&a.tm_dq, sDQ, 0, q0, bh);
     }
-    if (leader) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
 
   tc_fence_before();
@@ -407,43 +387,58 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
   }
 }
 
-// One warp per row of the padded [B*H, n_pad] layout.  Rows q < N: -D with
-// D = rowsum(dO * O), -LSE * log2(e), and dQ := 0.  Padding rows q >= N: -inf and 0,
-// so that a query past the end contributes P = 0.
+// b as three bf16 terms b1 + b2 + b3 (each the rounding of what the previous ones
+// left), packed as the first three of eight bf16: about 24 significant bits.
+__device__ __forceinline__ uint4 bias_terms(float b) {
+  if (!isfinite(b)) return make_uint4(__bfloat16_as_ushort(__float2bfloat16_rn(b)), 0u, 0u, 0u);
+  const __nv_bfloat16 b1 = __float2bfloat16_rn(b);
+  const float r1 = b - __bfloat162float(b1);
+  const __nv_bfloat16 b2 = __float2bfloat16_rn(r1);
+  const float r2 = r1 - __bfloat162float(b2);
+  const __nv_bfloat16 b3 = __float2bfloat16_rn(r2);
+  return make_uint4(static_cast<uint32_t>(__bfloat16_as_ushort(b1)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b2)) << 16),
+                    static_cast<uint32_t>(__bfloat16_as_ushort(b3)), 0u, 0u);
+}
+
+// One warp per row of the padded [B*H, n_pad] layout.  Rows q < N: D = rowsum(dO * O),
+// the biases -LSE/scale and -D, and dQ := 0.  Padding rows q >= N: biases -inf and 0,
+// so that a query past the end contributes P = 0.  The biases go into the query
+// block's two bias tiles (64 rows x 16 bf16 each, no-swizzle K-major core matrices):
+// row r's 32 bytes are two 16-byte pieces, columns 0-7 and 8-15.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess(const void* __restrict__ o, int o_f32,
                                                        const __nv_bfloat16* __restrict__ dout,
-                                                       const float* __restrict__ lse, float* __restrict__ neg_lse2,
-                                                       float* __restrict__ neg_delta, float* __restrict__ dq, int N,
-                                                       int n_pad, long long padded_rows) {
+                                                       const float* __restrict__ lse, uint8_t* __restrict__ bias,
+                                                       float* __restrict__ dq, int N, int n_pad, long long padded_rows,
+                                                       float inv_scale) {
   constexpr int kPer = D / 32;
   const long long prow = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (prow >= padded_rows) return;
   const long long bh = prow / n_pad;
   const int q = static_cast<int>(prow - bh * n_pad);
-  if (q >= N) {
-    if (lane == 0) {
-      neg_lse2[prow] = -INFINITY;
-      neg_delta[prow] = 0.f;
+  float bs = -INFINITY, bd = 0.f;
+  if (q < N) {
+    const long long row = bh * N + q;
+    const size_t base = static_cast<size_t>(row) * D + lane * kPer;
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const float ov = o_f32 ? static_cast<const float*>(o)[base + i]
+                             : __bfloat162float(static_cast<const __nv_bfloat16*>(o)[base + i]);
+      acc = fmaf(__bfloat162float(dout[base + i]), ov, acc);
+      dq[base + i] = 0.f;
     }
-    return;
-  }
-  const long long row = bh * N + q;
-  const size_t base = static_cast<size_t>(row) * D + lane * kPer;
-  float acc = 0.f;
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const float ov = o_f32 ? static_cast<const float*>(o)[base + i]
-                           : __bfloat162float(static_cast<const __nv_bfloat16*>(o)[base + i]);
-    acc = fmaf(__bfloat162float(dout[base + i]), ov, acc);
-    dq[base + i] = 0.f;
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    bs = -lse[row] * inv_scale;
+    bd = -acc;
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
-    neg_delta[prow] = -acc;
-    neg_lse2[prow] = -lse[row] * kLog2e;
+  if (lane < 4) {  // lane: tile (lane >> 1: 0 = LSE, 1 = D), piece (lane & 1)
+    const int r = q & (kBQ - 1);
+    uint8_t* tile = bias + (static_cast<size_t>(bh) * (n_pad / kBQ) + q / kBQ) * (2 * kBQ * 32) + (lane >> 1) * (kBQ * 32);
+    const int off = ((r >> 3) * 2 + (lane & 1)) * 128 + (r & 7) * 16;
+    *reinterpret_cast<uint4*>(tile + off) = (lane & 1) ? make_uint4(0u, 0u, 0u, 0u) : bias_terms((lane >> 1) ? bd : bs);
   }
 }
 
@@ -452,8 +447,8 @@ cudaError_t launch_bwd_t(const BackwardArgs& a, cudaStream_t stream) {
   using C = BwdCfg<D>;
   const long long padded_rows = static_cast<long long>(a.B) * a.H * a.n_pad;
   bwd_preprocess<D><<<static_cast<unsigned>((padded_rows + 7) / 8), 256, 0, stream>>>(
-      a.o, a.o_f32, static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.neg_lse2, a.neg_delta, a.dq, a.N, a.n_pad,
-      padded_rows);
+      a.o, a.o_f32, static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.bias, a.dq, a.N, a.n_pad, padded_rows,
+      1.f / a.scale);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);

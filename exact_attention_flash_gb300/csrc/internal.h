@@ -21,15 +21,14 @@ struct ForwardArgs {
 
 struct BackwardArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 3-D maps over [B*H, N, d] bf16; Q, dO boxes of 64 rows, K, V of 128
-  CUtensorMap tm_dq;                    // 3-D map over dQ [B*H, N, d] fp32, box {d, 64, 1}, for bulk reductions
   const void* o;                        // [B, H, N, d] bf16 or fp32
   const void* dout;                     // [B, H, N, d] bf16
   const float* lse;                     // [B, H, N]
   float* dq;                            // [B, H, N, d] fp32 (accumulated into; zeroed by the launcher)
   float* dk;                            // [B, H, N, d] fp32
   float* dv;                            // [B, H, N, d] fp32
-  float* neg_lse2;                      // workspace [B*H, n_pad]: -LSE * log2(e), -inf past N
-  float* neg_delta;                     // workspace [B*H, n_pad]: -rowsum(dO * O), 0 past N
+  uint8_t* bias;                        // workspace [B*H, n_pad / 64] blocks of 4 KB: per 64-query block the
+                                        // bias tiles -LSE/scale and -rowsum(dO * O) (-inf and 0 past N)
   int n_pad;                            // N rounded up to a multiple of 64
   int B, H, N, d;
   float scale;                          // softmax scale

@@ -72,8 +72,9 @@ const char* fa_status_string(fa_status s);
 fa_status fa_forward(const void* q, const void* k, const void* v, void* o, fa_dtype o_dtype, float* lse, int B,
                      int H, int N, int d, float scale, int causal, int precise, void* stream);
 
-/* Bytes of workspace fa_backward needs: per query row, D = rowsum(dO * O) and
- * the LSE in base 2, both over N rounded up to a multiple of 64. */
+/* Bytes of workspace fa_backward needs: 64 per query row over N rounded up to a
+ * multiple of 64 (per row, -LSE/scale and -rowsum(dO * O), each as three bf16
+ * terms, laid out as tensor-core operand tiles). */
 size_t fa_backward_workspace_size(int B, int H, int N, int d);
 
 /*

@@ -45,8 +45,9 @@ def test_version_and_status_strings(lib):
 
 
 def test_workspace_sizes(lib):
-    assert lib.fa_backward_workspace_size(2, 16, 8192, 128) == 2 * (2 * 16 * 8192 * 4)
-    assert lib.fa_backward_workspace_size(1, 1, 65, 64) == 2 * 512  # rows padded to 128 floats
+    # per query row (padded to a multiple of 64): two 32-byte rows of bias tiles
+    assert lib.fa_backward_workspace_size(2, 16, 8192, 128) == 2 * 16 * 8192 * 64
+    assert lib.fa_backward_workspace_size(1, 1, 65, 64) == 128 * 64  # rows padded to 128
     counters = ((16 * 32 * 4 + 255) // 256) * 256
     partials = 16 * 32 * 64 * 130 * 4
     assert lib.fa_decode_workspace_size(16, 32, 128, 64) == counters + ((partials + 255) // 256) * 256
