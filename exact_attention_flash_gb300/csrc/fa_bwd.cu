@@ -9,18 +9,23 @@
 // lie wholly before the key tile are skipped; the others are masked per element.
 //
 // Kernels:
-//   bwd_preprocess  one warp per row: D = rowsum(dO * O), and dQ := 0.
+//   bwd_preprocess  one warp per row: D = rowsum(dO * O), the per-query biases
+//                   -LSE/scale and -D as tensor-core operand tiles, and dQ := 0.
 //   bwd_kernel      one CTA per (128-key tile, batch*head); it walks the query
 //                   tiles of 64 rows.  Keys are the TMEM lanes, so the kernel
 //                   forms the transposed products:
-//       S^T = K Q_i^T and dP^T = V dO_i^T        (SS MMA, M=128, N=64)
+//       S^T = K Q_i^T - LSE_i/scale and dP^T = V dO_i^T - D_i
+//                                                (SS MMA, M=128, N=64; each
+//                                                 accumulator starts from a
+//                                                 K=16 bias product)
 //       dV += P^T dO_i and dK += dS^T Q_i        (TS MMA, A = P^T / dS^T in TMEM)
 //       dQ_i^T = K^T dS_i^T                      (SS MMA, M=d, N=64, dS from smem)
-//   warp 8 loads (TMA), warp 9 issues MMAs, warps 0-3 (thread = key) turn S^T,
-//   dP^T into P^T, dS^T, warps 4-7 (thread = feature) add dQ_i^T into dQ with
-//   fp32 reductions in L2.  S^T/dP^T are double-buffered in TMEM so the tensor
-//   core computes step n+1 while step n's elementwise work runs; dQ^T of step
-//   n lands in the dP^T buffer that dS^T of step n has just left.
+//   warp 16 loads (TMA), warp 17 issues MMAs, warps 0-7 (thread = key, two
+//   warpgroups by query half) turn S^T, dP^T into P^T, dS^T, warps 8-15 (thread =
+//   feature) add dQ_i^T into dQ with fp32 reductions in L2.  S^T/dP^T are
+//   double-buffered in TMEM so the tensor core computes step n+1 while step n's
+//   elementwise work runs; dQ^T of step n lands in the dP^T buffer that dS^T of
+//   step n has just left.
 // Tensor memory (512 columns): S^T[2] [0,64) [64,128), dP^T[2] [128,192)
 // [192,256), dV [256, 256+d), dK [256+d, 256+2d).
 #include <cuda_bf16.h>
