@@ -483,6 +483,58 @@ def run_profile_case(name, reps):
     print(json.dumps({"profile_case": name, **c, "reps": reps, "ms_per_call": e0.elapsed_time(e1) / reps}))
 
 
+def run_all_workloads(reps):
+    """One JSON line per named workload and kernel family: each call timed alone
+    with CUDA events (median of `reps`), with L2 flushed by a 256 MB write before
+    every timed call, so that small workloads are not timed from a warm L2."""
+    import statistics
+
+    from exact_attention_flash_gb300 import backward_workspace_bytes, fa_backward, fa_decode, fa_forward
+    from exact_attention_flash_gb300.build import build
+    from exact_attention_flash_gb300.workloads import WORKLOADS, make_attention_inputs, make_decode_inputs
+
+    build()
+    peaks = load_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for name, w in WORKLOADS.items():
+        calls = {}
+        if w.kind == "decode":
+            q, k, v = make_decode_inputs(w.B, w.H, w.N, w.d, w.seed, "cuda")
+            o, l = fa_decode(q, k, v, w.n_split)
+            calls["decode"] = (lambda: fa_decode(q, k, v, w.n_split, out=o, lse=l),  # noqa: E731
+                               decode_bytes(w.B, w.H, w.N, w.d, w.n_split), "GB/s")
+        else:
+            q, k, v, do = make_attention_inputs(w.B, w.H, w.N, w.d, w.seed, "cuda", qk_mult=w.qk_mult,
+                                                with_do=w.backward)
+            odt = torch.float32 if w.out_f32 else torch.bfloat16
+            o, lse = fa_forward(q, k, v, causal=w.causal, out_dtype=odt)
+            calls["forward"] = (lambda: fa_forward(q, k, v, causal=w.causal, out=o, lse=lse),  # noqa: E731
+                                attention_flops(w.B, w.H, w.N, w.d, w.causal, False), "TFLOP/s")
+            if w.backward:
+                ws = torch.empty(backward_workspace_bytes(w.B, w.H, w.N, w.d), device="cuda", dtype=torch.uint8)
+                calls["backward"] = (lambda: fa_backward(q, k, v, o, lse, do, causal=w.causal, workspace=ws),  # noqa: E731
+                                     attention_flops(w.B, w.H, w.N, w.d, w.causal, True), "TFLOP/s")
+        for kname, (fn, work, unit) in calls.items():
+            for _ in range(3):
+                fn()
+            times = []
+            for _ in range(reps):
+                flush.zero_()
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1))
+            ms = statistics.median(times)
+            rate = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
+            peak = peaks["bf16_tflops"] if unit == "TFLOP/s" else peaks["hbm_gbs"]
+            print(json.dumps({"workload": name, "kernel": kname, "ms": ms, "rate": rate, "unit": unit,
+                              "frac_of_measured_peak": rate / peak, "reps": reps, "l2": "flushed before each call"}))
+        del calls
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -492,9 +544,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--profile", choices=sorted(PROFILE_CASES), help="run one kernel on a reduced case (for ncu)")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--all-workloads", action="store_true",
+                    help="time every named workload's kernels alone (one JSON line each)")
     args = ap.parse_args()
     if args.profile:
         run_profile_case(args.profile, args.reps)
+        return
+    if args.all_workloads:
+        run_all_workloads(max(args.reps, 5))
         return
     world, rank, local = dist_setup(args)
     try:

@@ -40,6 +40,7 @@ __device__ unsigned g_fwd_status;
 constexpr int kBM = 128;             // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;             // keys per KV tile
 constexpr int kTiles = 2;            // query tiles per CTA
+constexpr int kHeadGroup = 8;        // heads whose blocks are interleaved in the grid order
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kFwdThreads = 384;  // warps 10-11 only lend their registers to the softmax warps
@@ -89,11 +90,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  // Head-major order: the query blocks of one head run side by side and share
-  // its K and V in L2; within a head the heaviest (latest) causal block starts first.
+  // Block order: heads in groups of kHeadGroup; within a group, the query blocks
+  // go latest first across the group's heads (under causality the latest block
+  // has the most key tiles).  The longest blocks start first, which shortens the
+  // tail of the grid, while only a group's K and V need to stay in L2.
   const int n_qblk = (a.N + kBM * kTiles - 1) / (kBM * kTiles);
-  const int bh = blockIdx.x / n_qblk;
-  const int q_row0 = (n_qblk - 1 - static_cast<int>(blockIdx.x % n_qblk)) * (kBM * kTiles);
+  const int n_bh = a.B * a.H;
+  const int per_group = kHeadGroup * n_qblk;
+  const int group = static_cast<int>(blockIdx.x) / per_group;
+  const int g_heads = min(kHeadGroup, n_bh - group * kHeadGroup);  // the last group may be smaller
+  const int g_idx = static_cast<int>(blockIdx.x) - group * per_group;
+  const int bh = group * kHeadGroup + g_idx % g_heads;
+  const int q_row0 = (n_qblk - 1 - g_idx / g_heads) * (kBM * kTiles);
   const int n_kv_total = (a.N + kBN - 1) / kBN;
   int n_kv[kTiles];
 #pragma unroll
