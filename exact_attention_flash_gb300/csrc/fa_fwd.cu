@@ -26,6 +26,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -36,6 +37,11 @@ namespace fa {
 namespace {
 
 __device__ unsigned g_fwd_status;
+// Scheduling slots of the persistent forward: {items claimed, CTAs finished}.  Each
+// launch takes the next slot in turn, so launches that overlap on different
+// streams count on different slots; each launch leaves its slot at zero.
+constexpr int kSchedSlots = 64;
+__device__ unsigned g_fwd_sched[kSchedSlots][2];
 
 constexpr int kBM = 128;             // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;             // keys per KV tile
@@ -69,14 +75,47 @@ struct FwdCfg {
   static constexpr int kSmemBytes = kTiles * kTileBytes + kStages * 2 * kTileBytes + 1024;
 };
 
+constexpr int kItemRing = 2;
+constexpr int kItemReaders = 32 + 2 * kBM;  // the MMA warp and the softmax warps
+
 struct FwdBarriers {
-  uint64_t q_full;
+  uint64_t item_full[kItemRing], item_empty[kItemRing];
+  int item[kItemRing];
+  uint64_t q_full[kTiles], q_empty[kTiles];
   uint64_t k_full[4], v_full[4], kv_empty[4];
-  uint64_t s_full[kTiles], p_half[kTiles], p_full[kTiles], o_full[kTiles];
+  uint64_t s_full[kTiles], p_half[kTiles], p_full[kTiles], o_full[kTiles], o_empty[kTiles];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
+
+// One work item: kTiles * kBM query rows of one (batch, head), and the number of
+// key tiles each of its query tiles visits.
+struct FwdItem {
+  int bh, q_row0;
+  int n_kv[kTiles];
+};
+
+// Work items in dispatch order: heads in groups of kHeadGroup; within a group, the
+// query blocks go latest first across the group's heads (under causality the latest
+// block has the most key tiles).  The longest items start first, which shortens the
+// tail, while only a group's K and V need to stay in L2.
+__device__ __forceinline__ FwdItem fwd_item(const ForwardArgs& a, int item) {
+  const int n_qblk = (a.N + kBM * kTiles - 1) / (kBM * kTiles);
+  const int n_bh = a.B * a.H;
+  const int per_group = kHeadGroup * n_qblk;
+  const int group = item / per_group;
+  const int g_heads = min(kHeadGroup, n_bh - group * kHeadGroup);  // the last group may be smaller
+  const int g_idx = item - group * per_group;
+  FwdItem w;
+  w.bh = group * kHeadGroup + g_idx % g_heads;
+  w.q_row0 = (n_qblk - 1 - g_idx / g_heads) * (kBM * kTiles);
+  const int n_kv_total = (a.N + kBN - 1) / kBN;
+#pragma unroll
+  for (int t = 0; t < kTiles; ++t)
+    w.n_kv[t] = a.causal ? min(n_kv_total, (w.q_row0 + t * kBM) / kBN + 1) : n_kv_total;
+  return w;
+}
 
 template <int D, bool kPrecise>
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ ForwardArgs a) {
@@ -90,28 +129,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  // Block order: heads in groups of kHeadGroup; within a group, the query blocks
-  // go latest first across the group's heads (under causality the latest block
-  // has the most key tiles).  The longest blocks start first, which shortens the
-  // tail of the grid, while only a group's K and V need to stay in L2.
-  const int n_qblk = (a.N + kBM * kTiles - 1) / (kBM * kTiles);
-  const int n_bh = a.B * a.H;
-  const int per_group = kHeadGroup * n_qblk;
-  const int group = static_cast<int>(blockIdx.x) / per_group;
-  const int g_heads = min(kHeadGroup, n_bh - group * kHeadGroup);  // the last group may be smaller
-  const int g_idx = static_cast<int>(blockIdx.x) - group * per_group;
-  const int bh = group * kHeadGroup + g_idx % g_heads;
-  const int q_row0 = (n_qblk - 1 - g_idx / g_heads) * (kBM * kTiles);
-  const int n_kv_total = (a.N + kBN - 1) / kBN;
-  int n_kv[kTiles];
-#pragma unroll
-  for (int t = 0; t < kTiles; ++t)
-    n_kv[t] = a.causal ? min(n_kv_total, (q_row0 + t * kBM) / kBN + 1) : n_kv_total;
-  const int n_kv_cta = n_kv[kTiles - 1];
+  // Persistent: the producer claims items in dispatch order from a global counter
+  // (whichever CTA is free takes the next, longest first) and passes each index to
+  // the MMA issuer and the softmax warps through a two-slot ring.  The barriers'
+  // phases run on across items (one K/V ring, per-tile step counters, one Q and O
+  // hand-off per item).
+  const int n_items = a.B * a.H * ((a.N + kBM * kTiles - 1) / (kBM * kTiles));
 
   if (tid == 0) {
     bars.abort = 0;
-    mbar_init(&bars.q_full, 1);
+    for (int r = 0; r < kItemRing; ++r) {
+      mbar_init(&bars.item_full[r], 1);
+      mbar_init(&bars.item_empty[r], kItemReaders);
+    }
+    for (int t = 0; t < kTiles; ++t) {
+      mbar_init(&bars.q_full[t], 1);
+      mbar_init(&bars.q_empty[t], 1);
+      mbar_init(&bars.o_empty[t], kBM);
+    }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars.k_full[s], 1);
       mbar_init(&bars.v_full[s], 1);
@@ -142,31 +177,57 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         tma_prefetch_desc(&a.tm_q);
         tma_prefetch_desc(&a.tm_k);
         tma_prefetch_desc(&a.tm_v);
-        mbar_arrive_expect_tx(&bars.q_full, kTiles * C::kTileBytes);
-        for (int t = 0; t < kTiles; ++t)
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(sQ + t * C::kTileBytes + c * (kBM * 128), &a.tm_q, &bars.q_full, c * 64, q_row0 + t * kBM, bh);
-        int issued = 0;
-        for (int j = 0; j < n_kv_cta; ++j) {
-          const int s = j % C::kStages;
-          if (j >= C::kStages && !mbar_wait(&bars.kv_empty[s], ((j / C::kStages) - 1) & 1, &bars.abort, &g_fwd_status))
+        int g = 0;                     // K/V tiles issued (the ring position)
+        int q_issued[kTiles] = {0, 0};  // Q tiles issued per tile slot
+        bool ok = true;
+        for (int it = 0; ok; ++it) {
+          // Claim the next item and publish it (n_items once none is left).
+          const int r = it % kItemRing;
+          if (it >= kItemRing &&
+              !mbar_wait(&bars.item_empty[r], ((it / kItemRing) - 1) & 1, &bars.abort, &g_fwd_status))
             break;
-          uint8_t* k_dst = sK + s * C::kTileBytes;
-          uint8_t* v_dst = sV + s * C::kTileBytes;
-          mbar_arrive_expect_tx(&bars.k_full[s], C::kTileBytes);
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(k_dst + c * (kBN * 128), &a.tm_k, &bars.k_full[s], c * 64, j * kBN, bh);
-          mbar_arrive_expect_tx(&bars.v_full[s], C::kTileBytes);
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(v_dst + c * (kBN * 128), &a.tm_v, &bars.v_full[s], c * 64, j * kBN, bh);
-          ++issued;
+          const unsigned claimed = atomicAdd(a.sched, 1u);
+          const int item = claimed < static_cast<unsigned>(n_items) ? static_cast<int>(claimed) : n_items;
+          bars.item[r] = item;
+          mbar_arrive(&bars.item_full[r]);
+          if (item >= n_items) break;
+          const FwdItem w = fwd_item(a, item);
+          // Q tile t is reloaded once the previous item's last S_t product has read it.
+          for (int t = 0; ok && t < kTiles; ++t) {
+            if (it > 0 && !mbar_wait(&bars.q_empty[t], (it - 1) & 1, &bars.abort, &g_fwd_status)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&bars.q_full[t], C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_3d(sQ + t * C::kTileBytes + c * (kBM * 128), &a.tm_q, &bars.q_full[t], c * 64,
+                          w.q_row0 + t * kBM, w.bh);
+            ++q_issued[t];
+          }
+          for (int j = 0; ok && j < w.n_kv[kTiles - 1]; ++j) {
+            const int s = g % C::kStages;
+            if (g >= C::kStages && !mbar_wait(&bars.kv_empty[s], ((g / C::kStages) - 1) & 1, &bars.abort, &g_fwd_status)) {
+              ok = false;
+              break;
+            }
+            uint8_t* k_dst = sK + s * C::kTileBytes;
+            uint8_t* v_dst = sV + s * C::kTileBytes;
+            mbar_arrive_expect_tx(&bars.k_full[s], C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_3d(k_dst + c * (kBN * 128), &a.tm_k, &bars.k_full[s], c * 64, j * kBN, w.bh);
+            mbar_arrive_expect_tx(&bars.v_full[s], C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_3d(v_dst + c * (kBN * 128), &a.tm_v, &bars.v_full[s], c * 64, j * kBN, w.bh);
+            ++g;
+          }
         }
         // Drain: every copy this CTA started must land before shared memory is released.
-        mbar_wait_drain(&bars.q_full, 0);
-        for (int j = max(0, issued - C::kStages); j < issued; ++j) {
-          const int s = j % C::kStages;
-          mbar_wait_drain(&bars.k_full[s], (j / C::kStages) & 1);
-          mbar_wait_drain(&bars.v_full[s], (j / C::kStages) & 1);
+        for (int t = 0; t < kTiles; ++t)
+          if (q_issued[t] > 0) mbar_wait_drain(&bars.q_full[t], (q_issued[t] - 1) & 1);
+        for (int gg = max(0, g - C::kStages); gg < g; ++gg) {
+          const int s = gg % C::kStages;
+          mbar_wait_drain(&bars.k_full[s], (gg / C::kStages) & 1);
+          mbar_wait_drain(&bars.v_full[s], (gg / C::kStages) & 1);
         }
       }
       __syncwarp();
@@ -181,8 +242,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         const uint64_t dQ = sdesc_sw128(smem_u32(sQ), 16, 1024);         // Q tile 0, K-major
         const uint64_t dK = sdesc_sw128(smem_u32(sK), 16, 1024);         // K stage 0, K-major
         const uint64_t dV = sdesc_sw128(smem_u32(sV), kBN * 128, 1024);  // V stage 0, MN-major
-        auto issue_s = [&](int t, int j) {
-          const int s = j % C::kStages;
+        auto issue_s = [&](int t, int s) {  // S_t from the K tile in ring stage s
           const uint64_t q_d = desc_add(dQ, t * C::kTileBytes), k_d = desc_add(dK, s * C::kTileBytes);
           const uint32_t s_tm = tmem + t * kBN;
   #pragma unroll
@@ -193,18 +253,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           umma_commit(&bars.s_full[t], leader);
         };
         // O_t += P_t V_j in two halves of 64 keys: the softmax releases P's first
-        // half (p_half) while it still computes the second (p_full).
-        auto issue_pv = [&](int t, int j) -> bool {
-          const int s = j % C::kStages;
+        // half (p_half) while it still computes the second (p_full).  s: ring stage of
+        // V_j; step: the tile's step count across items (the P barriers' phase);
+        // first: the item's first key tile (O is written, not accumulated).
+        auto issue_pv = [&](int t, int s, int step, bool first) -> bool {
           const uint64_t v_d = desc_add(dV, s * C::kTileBytes);
           const uint32_t o_tm = tmem + C::kOCol + t * D, p_tm = tmem + t * kBN;
-          const uint32_t acc0 = j > 0 ? 1u : 0u;
-          if (!warp_wait(&bars.p_half[t], j & 1, &bars.abort, &g_fwd_status)) return false;
+          const uint32_t acc0 = first ? 0u : 1u;
+          if (!warp_wait(&bars.p_half[t], step & 1, &bars.abort, &g_fwd_status)) return false;
           tc_fence_after();
   #pragma unroll
           for (int kk = 0; kk < kBN / 32; ++kk)
             umma_ts(o_tm, p_tm + kk * 8, desc_add(v_d, kk * 16 * 128), kIdO, kk > 0 ? 1u : acc0, leader);
-          if (!warp_wait(&bars.p_full[t], j & 1, &bars.abort, &g_fwd_status)) return false;
+          if (!warp_wait(&bars.p_full[t], step & 1, &bars.abort, &g_fwd_status)) return false;
           tc_fence_after();
   #pragma unroll
           for (int kk = kBN / 32; kk < kBN / 16; ++kk)
@@ -216,37 +277,60 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           }
           return true;
         };
-        bool ok = warp_wait(&bars.q_full, 0, &bars.abort, &g_fwd_status) &&
-                  warp_wait(&bars.k_full[0], 0, &bars.abort, &g_fwd_status);
-        if (ok) {
-          tc_fence_after();
-          for (int t = 0; t < kTiles; ++t) issue_s(t, 0);
-        }
-        for (int j = 0; ok && j < n_kv_cta; ++j) {
-          const int s = j % C::kStages;
-          const int jn = j + 1, sn = jn % C::kStages;
-          if (!warp_wait(&bars.v_full[s], (j / C::kStages) & 1, &bars.abort, &g_fwd_status)) break;
-          // tile 0
-          if (j < n_kv[0]) {
-            if (!issue_pv(0, j)) break;
-            if (jn < n_kv[0]) {
-              if (!warp_wait(&bars.k_full[sn], (jn / C::kStages) & 1, &bars.abort, &g_fwd_status)) break;
-              tc_fence_after();
-              issue_s(0, jn);
-            } else {
-              umma_commit(&bars.o_full[0], leader);
+        int g = 0;                  // K/V tiles consumed (the ring position)
+        int step[kTiles] = {0, 0};  // per-tile steps before the current item
+        bool ok = true;
+        for (int it = 0; ok; ++it) {
+          const int r = it % kItemRing;
+          if (!warp_wait(&bars.item_full[r], (it / kItemRing) & 1, &bars.abort, &g_fwd_status)) break;
+          const int item = bars.item[r];
+          mbar_arrive(&bars.item_empty[r]);
+          if (item >= n_items) break;
+          const FwdItem w = fwd_item(a, item);
+          const int s0 = g % C::kStages;
+          ok = warp_wait(&bars.k_full[s0], (g / C::kStages) & 1, &bars.abort, &g_fwd_status);
+          for (int t = 0; ok && t < kTiles; ++t) {
+            if (!warp_wait(&bars.q_full[t], it & 1, &bars.abort, &g_fwd_status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(t, s0);
+          }
+          for (int j = 0; ok && j < w.n_kv[kTiles - 1]; ++j, ++g) {
+            const int s = g % C::kStages, sn = (g + 1) % C::kStages;
+            const uint32_t phn = ((g + 1) / C::kStages) & 1;
+            if (!warp_wait(&bars.v_full[s], (g / C::kStages) & 1, &bars.abort, &g_fwd_status)) {
+              ok = false;
+              break;
+            }
+            for (int t = 0; t < kTiles; ++t) {
+              if (j >= w.n_kv[t]) continue;  // tile 0 may need one key tile fewer
+              // The item's first P V_t overwrites O_t: the previous item's epilogue must
+              // have read O_t out of tensor memory.
+              if (j == 0 && it > 0 && !warp_wait(&bars.o_empty[t], (it - 1) & 1, &bars.abort, &g_fwd_status)) {
+                ok = false;
+                break;
+              }
+              if (!issue_pv(t, s, step[t] + j, j == 0)) {
+                ok = false;
+                break;
+              }
+              if (t == kTiles - 1) umma_commit(&bars.kv_empty[s], leader);
+              if (j + 1 < w.n_kv[t]) {
+                if (!warp_wait(&bars.k_full[sn], phn, &bars.abort, &g_fwd_status)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                issue_s(t, sn);
+              } else {
+                umma_commit(&bars.o_full[t], leader);   // O_t of this item is complete
+                umma_commit(&bars.q_empty[t], leader);  // its last S_t product has read Q_t
+              }
             }
           }
-          // tile 1
-          if (!issue_pv(1, j)) break;
-          umma_commit(&bars.kv_empty[s], leader);
-          if (jn < n_kv[1]) {
-            if (!warp_wait(&bars.k_full[sn], (jn / C::kStages) & 1, &bars.abort, &g_fwd_status)) break;
-            tc_fence_after();
-            issue_s(1, jn);
-          } else {
-            umma_commit(&bars.o_full[1], leader);
-          }
+          for (int t = 0; t < kTiles; ++t) step[t] += w.n_kv[t];
         }
         // Drain: all MMAs complete before tensor memory is released.
         umma_commit(&bars.drain, leader);
@@ -260,17 +344,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     const int t = warp >> 2;                  // query tile of this warpgroup
     const int r = tid - t * kBM;              // row within the tile == TMEM lane
     const int lane_base = (warp & 3) * 32;    // TMEM lane quarter of this warp
-    const int row = q_row0 + t * kBM + r;
     const uint32_t s_tm = tmem_addr(tmem, lane_base, t * kBN);
     const uint32_t o_tm = tmem_addr(tmem, lane_base, C::kOCol + t * D);
     const float sl2 = a.scale_log2;
+    int step = 0;  // this tile's steps across items (the S and P barriers' phase)
+    bool ok = true;
+    for (int it = 0; ok; ++it) {
+    const int ring = it % kItemRing;
+    if (!__all_sync(0xffffffffu, mbar_wait(&bars.item_full[ring], (it / kItemRing) & 1, &bars.abort, &g_fwd_status)))
+      break;
+    const int item = bars.item[ring];
+    mbar_arrive(&bars.item_empty[ring]);
+    if (item >= n_items) break;
+    const FwdItem w = fwd_item(a, item);
+    const int q_row0 = w.q_row0, bh = w.bh;
+    const int row = q_row0 + t * kBM + r;
     float m_run = -INFINITY;  // reference max (scaled, log2 units)
     float l_run = 0.f;  // sum of p: the log-sum-exp
     float l_hat = 0.f;  // sum of the bf16-rounded p that enter P V: the normaliser of O
-    bool ok = true;
-    for (int j = 0; j < n_kv[t]; ++j) {
+    for (int j = 0; j < w.n_kv[t]; ++j, ++step) {
       // Lanes leave together: the TMEM accesses below are warp-collective.
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars.s_full[t], j & 1, &bars.abort, &g_fwd_status))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars.s_full[t], step & 1, &bars.abort, &g_fwd_status))) {
         ok = false;
         break;
       }
@@ -380,13 +474,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       mbar_arrive(&bars.p_full[t]);
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && __all_sync(0xffffffffu, mbar_wait(&bars.o_full[t], 0, &bars.abort, &g_fwd_status))) {
-      tc_fence_after();
+    // The whole O row leaves tensor memory first; o_empty then lets the next item's
+    // first P V product overwrite it while this row is normalised and stored.
+    if (!ok || !__all_sync(0xffffffffu, mbar_wait(&bars.o_full[t], it & 1, &bars.abort, &g_fwd_status))) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    uint32_t orow[D];
+#pragma unroll
+    for (int c = 0; c < D; c += 64) {
+      uint32_t (&part)[64] = *reinterpret_cast<uint32_t (*)[64]>(orow + c);
+      tmem_ld64(o_tm + c, part);
+    }
+    tc_fence_before();
+    mbar_arrive(&bars.o_empty[t]);
+    {
       const float inv_l = 1.f / l_hat;
       const size_t row_off = (static_cast<size_t>(bh) * a.N + row) * D;
+#pragma unroll
       for (int c = 0; c < D; c += 32) {
-        uint32_t u[32];
-        tmem_ld32(o_tm + c, u);
+        const uint32_t* u = orow + c;
         if (row < a.N) {
           if (a.o_f32) {
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.o) + row_off + c);
@@ -409,6 +517,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       }
       if (row < a.N) a.lse[static_cast<size_t>(bh) * a.N + row] = (m_run + __log2f(l_run)) * kLn2;
     }
+    }
   }
 
   tc_fence_before();
@@ -416,6 +525,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  }
+  // The last CTA to finish returns the scheduling slot to zero for its next launch.
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
+      atomicExch(a.sched, 0u);
+      atomicExch(a.sched + 1, 0u);
+    }
   }
 }
 
@@ -431,10 +548,23 @@ cudaError_t launch_fwd_t(const ForwardArgs& a, cudaStream_t stream) {
   e = cudaFuncGetAttributes(&attr, fwd_kernel<D, kPrecise>);
   if (e != cudaSuccess) return e;
   if (attr.numRegs * kFwdThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
-  const long long ctas = static_cast<long long>(a.B) * a.H * ((a.N + kBM * kTiles - 1) / (kBM * kTiles));
-  if (ctas > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-  dim3 grid(static_cast<unsigned>(ctas));
-  fwd_kernel<D, kPrecise><<<grid, kFwdThreads, C::kSmemBytes, stream>>>(a);
+  const long long items = static_cast<long long>(a.B) * a.H * ((a.N + kBM * kTiles - 1) / (kBM * kTiles));
+  if (items > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  // Persistent grid: one CTA per SM (each needs a whole SM's tensor memory), each
+  // walking its share of the items.
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  dim3 grid(static_cast<unsigned>(items < sms ? items : sms));
+  static std::atomic<unsigned> next_slot{0};
+  void* slots = nullptr;
+  e = cudaGetSymbolAddress(&slots, g_fwd_sched);
+  if (e != cudaSuccess) return e;
+  ForwardArgs args = a;
+  args.sched = static_cast<unsigned*>(slots) + 2 * (next_slot.fetch_add(1u) % kSchedSlots);
+  fwd_kernel<D, kPrecise><<<grid, kFwdThreads, C::kSmemBytes, stream>>>(args);
   return cudaGetLastError();
 }
 

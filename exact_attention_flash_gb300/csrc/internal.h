@@ -17,6 +17,7 @@ struct ForwardArgs {
   int causal;
   int o_f32;                     // 1: O is fp32, 0: bf16
   int precise;                   // 1: P enters PV as a bf16 hi + lo pair (two MMAs)
+  unsigned* sched;               // set by the launcher: {items claimed, CTAs finished}, zero between launches
 };
 
 struct BackwardArgs {
