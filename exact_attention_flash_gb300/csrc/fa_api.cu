@@ -97,6 +97,7 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, fa_dt
   a.d = d;
   a.scale_log2 = resolve_scale(scale, d) * kLog2e;
   a.causal = causal ? 1 : 0;
+  a.head_group = fa::head_group_for(a.causal, 2ll * N * d * 2, B * H);  // K and V of a head, bf16
   a.o_f32 = (o_dtype == FA_F32) ? 1 : 0;
   a.precise = precise ? 1 : 0;
   return fa::launch_forward(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -144,6 +145,7 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   a.scale = resolve_scale(scale, d);
   a.scale_log2 = a.scale * kLog2e;
   a.causal = causal ? 1 : 0;
+  a.head_group = fa::head_group_for(a.causal, 2ll * N * d * 2 + static_cast<long long>(N) * d * 4, B * H);  // Q, dO, dQ
   a.o_f32 = (o_dtype == FA_F32) ? 1 : 0;
   const cudaError_t e = fa::launch_backward(a, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;

@@ -44,7 +44,6 @@ __device__ unsigned g_bwd_status;
 
 constexpr int kBKV = 128;  // keys per CTA
 constexpr int kBQ = 64;    // queries per step
-constexpr int kHeadGroup = 8;  // heads whose blocks are interleaved in the grid order
 // Warps 0-7: P^T / dS^T and warps 8-15: dQ writers (each two warpgroups, one per
 // half of the step's 64 query columns); warp 16: TMA producer; warp 17: MMA
 // issuer; warps 18-19 only lend their registers.
@@ -107,17 +106,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  // Block order: heads in groups of kHeadGroup; within a group, the key tiles go
+  // Block order: heads in groups of a.head_group; within a group, the key tiles go
   // first to last across the group's heads (under causality key tile 0 meets the
   // most query tiles).  The longest blocks start first, which shortens the tail of
   // the grid, while only a group's Q, dO and dQ need to stay in L2.
   const int n_kv = (a.N + kBKV - 1) / kBKV;
   const int n_bh = a.B * a.H;
-  const int per_group = kHeadGroup * n_kv;
+  const int hg = a.head_group;
+  const int per_group = hg * n_kv;
   const int group = static_cast<int>(blockIdx.x) / per_group;
-  const int g_heads = min(kHeadGroup, n_bh - group * kHeadGroup);  // the last group may be smaller
+  const int g_heads = min(hg, n_bh - group * hg);  // the last group may be smaller
   const int g_idx = static_cast<int>(blockIdx.x) - group * per_group;
-  const int bh = group * kHeadGroup + g_idx % g_heads;
+  const int bh = group * hg + g_idx % g_heads;
   const int j = g_idx / g_heads;
   const int key0 = j * kBKV;
   const int n_q = (a.N + kBQ - 1) / kBQ;

@@ -46,7 +46,6 @@ __device__ unsigned g_fwd_sched[kSchedSlots][2];
 constexpr int kBM = 128;             // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;             // keys per KV tile
 constexpr int kTiles = 2;            // query tiles per CTA
-constexpr int kHeadGroup = 8;        // heads whose blocks are interleaved in the grid order
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kFwdThreads = 384;  // warps 10-11 only lend their registers to the softmax warps
@@ -96,19 +95,20 @@ struct FwdItem {
   int n_kv[kTiles];
 };
 
-// Work items in dispatch order: heads in groups of kHeadGroup; within a group, the
+// Work items in dispatch order: heads in groups of a.head_group; within a group, the
 // query blocks go latest first across the group's heads (under causality the latest
 // block has the most key tiles).  The longest items start first, which shortens the
 // tail, while only a group's K and V need to stay in L2.
 __device__ __forceinline__ FwdItem fwd_item(const ForwardArgs& a, int item) {
   const int n_qblk = (a.N + kBM * kTiles - 1) / (kBM * kTiles);
   const int n_bh = a.B * a.H;
-  const int per_group = kHeadGroup * n_qblk;
+  const int hg = a.head_group;
+  const int per_group = hg * n_qblk;
   const int group = item / per_group;
-  const int g_heads = min(kHeadGroup, n_bh - group * kHeadGroup);  // the last group may be smaller
+  const int g_heads = min(hg, n_bh - group * hg);  // the last group may be smaller
   const int g_idx = item - group * per_group;
   FwdItem w;
-  w.bh = group * kHeadGroup + g_idx % g_heads;
+  w.bh = group * hg + g_idx % g_heads;
   w.q_row0 = (n_qblk - 1 - g_idx / g_heads) * (kBM * kTiles);
   const int n_kv_total = (a.N + kBN - 1) / kBN;
 #pragma unroll

@@ -18,6 +18,7 @@ struct ForwardArgs {
   int o_f32;                     // 1: O is fp32, 0: bf16
   int precise;                   // 1: P enters PV as a bf16 hi + lo pair (two MMAs)
   unsigned* sched;               // set by the launcher: {items claimed, CTAs finished}, zero between launches
+  int head_group;                // heads interleaved in the work order (set by the API, see head_group_for)
 };
 
 struct BackwardArgs {
@@ -36,7 +37,23 @@ struct BackwardArgs {
   float scale_log2;                     // scale * log2(e)
   int causal;
   int o_f32;
+  int head_group;                       // heads interleaved in the grid order (set by the API, see head_group_for)
 };
+
+// Heads whose blocks are interleaved in the work order.  Under causality a block's
+// work grows with its position, and interleaving heads lets the longest blocks of
+// several heads start first, which shortens the tail; the interleaved heads' K and V
+// (forward) or Q, dO and dQ (backward) must then share L2, so a group holds as many
+// heads as fit a 64 MB budget, at most 8, and the heads are split into groups of
+// equal size (a small last group would start its longest blocks late).  Without
+// causality every block has the same work and one head at a time keeps the most in L2.
+inline int head_group_for(int causal, long long bytes_per_head, int n_bh) {
+  if (!causal || n_bh < 1) return 1;
+  long long fit = (64ll << 20) / (bytes_per_head > 0 ? bytes_per_head : 1);
+  fit = fit < 1 ? 1 : (fit > 8 ? 8 : fit);
+  const long long groups = (n_bh + fit - 1) / fit;
+  return static_cast<int>((n_bh + groups - 1) / groups);
+}
 
 struct DecodeArgs {
   const void* q;         // [B, H, 1, d] bf16

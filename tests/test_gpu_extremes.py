@@ -73,3 +73,38 @@ def test_decode_long_ragged_context():
     assert max_abs(f64(o), ref_o) <= O_MAX_ABS
     assert max_abs(f64(lse), ref_l[..., 0]) <= LSE_MAX_ABS
     assert np.isfinite(f64(o)).all()
+
+
+def test_forward_concurrent_streams_and_slot_reuse():
+    """The persistent forward claims work items from one of a rotating set of
+    scheduling slots.  Launches overlapping on four streams (different inputs)
+    must each be complete and correct, and 130 launches in a row (every slot
+    reused) must keep returning the same result."""
+    from exact_attention_flash_gb300 import fa_device_status, fa_forward
+    from exact_attention_flash_gb300.workloads import make_attention_inputs
+
+    inputs = [make_attention_inputs(1, 4, 1000, 128, 40 + i, "cuda", with_do=False)[:3] for i in range(4)]
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    outs = [None] * 4
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for i, (st, (q, k, v)) in enumerate(zip(streams, inputs)):
+            with torch.cuda.stream(st):
+                outs[i] = fa_forward(q, k, v, causal=bool(i & 1), stream=st)
+    torch.cuda.synchronize()
+    assert fa_device_status() == 0
+    for i, (q, k, v) in enumerate(inputs):
+        o, lse = outs[i]
+        rows = [0, 1, 255, 256, 511, 512, 999]
+        for h in (0, 3):
+            ref_o, ref_l = attention_dense_rows(f64(q[0, h]), f64(k[0, h]), f64(v[0, h]), rows, causal=bool(i & 1))
+            assert o_within_bar(f64(o[0, h, rows]), ref_o, "bf16") <= 0.0
+            assert max_abs(f64(lse[0, h, rows]), ref_l) <= LSE_MAX_ABS
+    q, k, v = inputs[0]
+    o0, l0 = fa_forward(q, k, v)
+    o, lse = torch.empty_like(o0), torch.empty_like(l0)
+    for _ in range(130):
+        fa_forward(q, k, v, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert fa_device_status() == 0
+    assert torch.equal(o, o0) and torch.equal(lse, l0)
