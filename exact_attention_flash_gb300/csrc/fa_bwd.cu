@@ -413,7 +413,8 @@ __device__ __forceinline__ uint4 bias_terms(float b) {
                     static_cast<uint32_t>(__bfloat16_as_ushort(b3)), 0u, 0u);
 }
 
-// One warp per row of the padded [B*H, n_pad] layout.  Rows q < N: D = rowsum(dO * O),
+// D/8 lanes per row of the padded [B*H, n_pad] layout (several rows per warp),
+// each lane owning 8 features in 16-byte accesses.  Rows q < N: D = rowsum(dO * O),
 // the biases -LSE/scale and -D, and dQ := 0.  Padding rows q >= N: biases -inf and 0,
 // so that a query past the end contributes P = 0.  The biases go into the query
 // block's two bias tiles (64 rows x 16 bf16 each, no-swizzle K-major core matrices):
@@ -424,34 +425,51 @@ __global__ void __launch_bounds__(256) bwd_preprocess(const void* __restrict__ o
                                                        const float* __restrict__ lse, uint8_t* __restrict__ bias,
                                                        float* __restrict__ dq, int N, int n_pad, long long padded_rows,
                                                        float inv_scale) {
-  constexpr int kPer = D / 32;
-  const long long prow = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (prow >= padded_rows) return;
-  const long long bh = prow / n_pad;
-  const int q = static_cast<int>(prow - bh * n_pad);
-  float bs = -INFINITY, bd = 0.f;
-  if (q < N) {
-    const long long row = bh * N + q;
-    const size_t base = static_cast<size_t>(row) * D + lane * kPer;
-    float acc = 0.f;
+  constexpr int kLanes = D / 8;                 // lanes per row
+  constexpr int kRowsPerBlock = 256 / kLanes;
+  const int sub = threadIdx.x % kLanes;         // 8-feature slice of the row
+  const long long prow = static_cast<long long>(blockIdx.x) * kRowsPerBlock + threadIdx.x / kLanes;
+  const bool live = prow < padded_rows;
+  const long long bh = live ? prow / n_pad : 0;
+  const int q = live ? static_cast<int>(prow - bh * n_pad) : 0;
+  float acc = 0.f;
+  if (live && q < N) {
+    const size_t base = static_cast<size_t>(bh * N + q) * D + sub * 8;
+    const uint4 dv = *reinterpret_cast<const uint4*>(dout + base);
+    float ov[8];
+    if (o_f32) {
+      const float4 a = *reinterpret_cast<const float4*>(static_cast<const float*>(o) + base);
+      const float4 b = *reinterpret_cast<const float4*>(static_cast<const float*>(o) + base + 4);
+      ov[0] = a.x; ov[1] = a.y; ov[2] = a.z; ov[3] = a.w; ov[4] = b.x; ov[5] = b.y; ov[6] = b.z; ov[7] = b.w;
+    } else {
+      const uint4 ob = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(o) + base);
+      const uint32_t w[4] = {ob.x, ob.y, ob.z, ob.w};
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const float ov = o_f32 ? static_cast<const float*>(o)[base + i]
-                             : __bfloat162float(static_cast<const __nv_bfloat16*>(o)[base + i]);
-      acc = fmaf(__bfloat162float(dout[base + i]), ov, acc);
-      dq[base + i] = 0.f;
+      for (int i = 0; i < 4; ++i) {
+        ov[2 * i] = __uint_as_float(w[i] << 16);
+        ov[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
     }
+    const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    bs = -lse[row] * inv_scale;
-    bd = -acc;
+    for (int i = 0; i < 4; ++i) {
+      acc = fmaf(__uint_as_float(dw[i] << 16), ov[2 * i], acc);
+      acc = fmaf(__uint_as_float(dw[i] & 0xFFFF0000u), ov[2 * i + 1], acc);
+    }
+    float4* z = reinterpret_cast<float4*>(dq + base);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  if (lane < 4) {  // lane: tile (lane >> 1: 0 = LSE, 1 = D), piece (lane & 1)
+  // Sum over the row's lanes (aligned groups of kLanes within the warp).
+#pragma unroll
+  for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (live && sub < 4) {  // sub: tile (sub >> 1: 0 = LSE, 1 = D), piece (sub & 1)
+    const float bs = q < N ? -lse[bh * N + q] * inv_scale : -INFINITY;
+    const float bd = q < N ? -acc : 0.f;
     const int r = q & (kBQ - 1);
-    uint8_t* tile = bias + (static_cast<size_t>(bh) * (n_pad / kBQ) + q / kBQ) * (2 * kBQ * 32) + (lane >> 1) * (kBQ * 32);
-    const int off = ((r >> 3) * 2 + (lane & 1)) * 128 + (r & 7) * 16;
-    *reinterpret_cast<uint4*>(tile + off) = (lane & 1) ? make_uint4(0u, 0u, 0u, 0u) : bias_terms((lane >> 1) ? bd : bs);
+    uint8_t* tile = bias + (static_cast<size_t>(bh) * (n_pad / kBQ) + q / kBQ) * (2 * kBQ * 32) + (sub >> 1) * (kBQ * 32);
+    const int off = ((r >> 3) * 2 + (sub & 1)) * 128 + (r & 7) * 16;
+    *reinterpret_cast<uint4*>(tile + off) = (sub & 1) ? make_uint4(0u, 0u, 0u, 0u) : bias_terms((sub >> 1) ? bd : bs);
   }
 }
 
@@ -459,7 +477,8 @@ template <int D>
 cudaError_t launch_bwd_t(const BackwardArgs& a, cudaStream_t stream) {
   using C = BwdCfg<D>;
   const long long padded_rows = static_cast<long long>(a.B) * a.H * a.n_pad;
-  bwd_preprocess<D><<<static_cast<unsigned>((padded_rows + 7) / 8), 256, 0, stream>>>(
+  constexpr int kRowsPerBlock = 256 / (D / 8);
+  bwd_preprocess<D><<<static_cast<unsigned>((padded_rows + kRowsPerBlock - 1) / kRowsPerBlock), 256, 0, stream>>>(
       a.o, a.o_f32, static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.bias, a.dq, a.N, a.n_pad, padded_rows,
       1.f / a.scale);
   cudaError_t e = cudaGetLastError();
