@@ -168,6 +168,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
           tma_load_3d(sK + c * (kBKV * 128), &a.tm_k, &sh.kv_full, c * 64, key0, bh);
           tma_load_3d(sV + c * (kBKV * 128), &a.tm_v, &sh.kv_full, c * 64, key0, bh);
         }
+        // The bias tiles come from the preprocess kernel, which may still be running.
+        griddep_wait();
         int issued = 0;
         for (int n = 0; n < n_steps; ++n) {
           const int s = n % C::kStages;
@@ -373,6 +375,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     const int lane_base = (warp & 3) * 32;
     const int c = lane_base + lane;               // feature index == TMEM lane of dQ^T
     const bool has_rows = lane_base < D;          // for d = 64, lanes 64..127 hold no feature
+    griddep_wait();  // dQ is zeroed by the preprocess kernel, which may still be running
     for (int n = 0; n < n_steps; ++n) {
       const int b = n & 1;
       const int q0 = (i_start + n) * kBQ + 32 * half;
@@ -427,6 +430,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess(const void* __restrict__ o
                                                        float inv_scale) {
   constexpr int kLanes = D / 8;                 // lanes per row
   constexpr int kRowsPerBlock = 256 / kLanes;
+  griddep_launch_dependents();  // the backward kernel may start its own setup meanwhile
   const int sub = threadIdx.x % kLanes;         // 8-feature slice of the row
   const long long prow = static_cast<long long>(blockIdx.x) * kRowsPerBlock + threadIdx.x / kLanes;
   const bool live = prow < padded_rows;
@@ -493,9 +497,20 @@ cudaError_t launch_bwd_t(const BackwardArgs& a, cudaStream_t stream) {
   if (attr.numRegs * kBwdThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
   const long long ctas = static_cast<long long>(a.B) * a.H * ((a.N + kBKV - 1) / kBKV);
   if (ctas > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-  dim3 grid(static_cast<unsigned>(ctas));
-  bwd_kernel<D><<<grid, kBwdThreads, C::kSmemBytes, stream>>>(a);
-  return cudaGetLastError();
+  // A programmatic dependent of the preprocess kernel: its CTAs set up (barriers,
+  // tensor memory, K and V) while the preprocess finishes, and wait for it only
+  // where they read what it wrote.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+  cfg.blockDim = dim3(kBwdThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr_pdl[1];
+  attr_pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr_pdl;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, bwd_kernel<D>, a);
 }
 
 }  // namespace

@@ -113,6 +113,14 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
   return true;
 }
 
+// ---------------------------------------------------------------- dependent launches
+// A kernel launched as a programmatic dependent of the previous one on its stream
+// may start before that one ends; griddep_wait blocks until the previous kernel has
+// completed and its writes are visible.  The previous kernel's
+// griddep_launch_dependents lets the dependent start as soon as SMs are free.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
