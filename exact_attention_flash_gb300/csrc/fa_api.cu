@@ -43,6 +43,21 @@ fa_status make_row_tile_map(CUtensorMap* m, const void* ptr, int BH, int N, int 
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// dK or dV [B*H, N, d] fp32 as a 3-D tensor, tiles of 128 rows x 32 features with the
+// 128-byte swizzle: the backward stores each key tile's gradients with bulk tensor
+// stores; rows past N are dropped.
+fa_status make_grad_store_map(CUtensorMap* m, void* ptr, int BH, int N, int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return FA_ERR_CUDA;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4};
+  const cuuint32_t box[3] = {32, 128, 1};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, elem,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -130,6 +145,8 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   if ((st = make_row_tile_map(&a.tm_k, k, BH, N, d, 128)) != FA_OK) return st;
   if ((st = make_row_tile_map(&a.tm_v, v, BH, N, d, 128)) != FA_OK) return st;
   if ((st = make_row_tile_map(&a.tm_do, dout, BH, N, d, 64)) != FA_OK) return st;
+  if ((st = make_grad_store_map(&a.tm_dk, dk, BH, N, d)) != FA_OK) return st;
+  if ((st = make_grad_store_map(&a.tm_dv, dv, BH, N, d)) != FA_OK) return st;
   a.o = o;
   a.dout = dout;
   a.lse = lse;

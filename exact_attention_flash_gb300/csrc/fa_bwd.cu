@@ -90,6 +90,18 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Bulk tensor store of a staged shared-memory box to global memory (rows past the
+// tensor's extent are dropped).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
+// Named barrier over the 256 P/dS threads.
+__device__ __forceinline__ void compute_bar_sync() { asm volatile("barrier.cta.sync 2, 256;" ::: "memory"); }
+
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_constant__ BackwardArgs a) {
   using C = BwdCfg<D>;
@@ -342,27 +354,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       mbar_arrive(&sh.p_full[b]);
     }
     // ------------------------------------------------------------ dK, dV epilogue
-    if (ok && __all_sync(0xffffffffu, mbar_wait(&sh.dkdv_full, 0, &sh.abort, &g_bwd_status))) {
+    // Once the last products are done, the Q/dO/dS buffers are free: dK and dV are
+    // staged there as [128 keys x 32 features] fp32 boxes with the 128-byte swizzle
+    // (16-byte piece j of row k at (j ^ (k % 8)) * 16, so that the staging stores
+    // spread over all banks) and leave with bulk tensor stores, one box per 32
+    // features.  Warpgroup h handles features [h d/2, (h + 1) d/2).
+    const bool e_ok = ok && __all_sync(0xffffffffu, mbar_wait(&sh.dkdv_full, 0, &sh.abort, &g_bwd_status));
+    if (e_ok) {
       tc_fence_after();
-      const size_t row_off = (static_cast<size_t>(bh) * a.N + key) * D;
-      // Warpgroup h stores feature columns [h d/2, (h + 1) d/2) of dK and dV.
+      constexpr int kBoxBytes = kBKV * 32 * 4;  // 16 KB
+      uint8_t* stage_v = sQ;                        // boxes of dV, then of dK
+      uint8_t* stage_k = sQ + (D / 32) * kBoxBytes;
 #pragma unroll 1
       for (int c = h * (D / 2); c < (h + 1) * (D / 2); c += 32) {
         uint32_t uv[32], uk[32];
         tmem_ld32(tmem_addr(tmem, lane_base, C::kDVCol + c), uv);
         tmem_ld32(tmem_addr(tmem, lane_base, C::kDKCol + c), uk);
-        if (key < a.N) {
-          float4* dv = reinterpret_cast<float4*>(a.dv + row_off + c);
-          float4* dkp = reinterpret_cast<float4*>(a.dk + row_off + c);
+        uint8_t* rv = stage_v + (c / 32) * kBoxBytes + k * 128;
+        uint8_t* rk = stage_k + (c / 32) * kBoxBytes + k * 128;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            dv[i] = make_float4(__uint_as_float(uv[4 * i]), __uint_as_float(uv[4 * i + 1]),
-                                __uint_as_float(uv[4 * i + 2]), __uint_as_float(uv[4 * i + 3]));
-            dkp[i] = make_float4(__uint_as_float(uk[4 * i]) * a.scale, __uint_as_float(uk[4 * i + 1]) * a.scale,
-                                 __uint_as_float(uk[4 * i + 2]) * a.scale, __uint_as_float(uk[4 * i + 3]) * a.scale);
-          }
+        for (int j = 0; j < 8; ++j) {
+          *reinterpret_cast<uint4*>(rv + ((j ^ (k & 7)) << 4)) = make_uint4(uv[4 * j], uv[4 * j + 1], uv[4 * j + 2], uv[4 * j + 3]);
+          *reinterpret_cast<float4*>(rk + ((j ^ (k & 7)) << 4)) =
+              make_float4(__uint_as_float(uk[4 * j]) * a.scale, __uint_as_float(uk[4 * j + 1]) * a.scale,
+                          __uint_as_float(uk[4 * j + 2]) * a.scale, __uint_as_float(uk[4 * j + 3]) * a.scale);
         }
       }
+      fence_proxy_async_smem();
+    }
+    compute_bar_sync();  // all boxes staged (or, after a failed wait, none)
+    if (e_ok && tid == 0) {
+      for (int i = 0; i < D / 32; ++i) {
+        tma_store_3d(&a.tm_dv, sQ + i * (kBKV * 32 * 4), 32 * i, key0, bh);
+        tma_store_3d(&a.tm_dk, sQ + (D / 32 + i) * (kBKV * 32 * 4), 32 * i, key0, bh);
+      }
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kWriterRegs));

@@ -23,6 +23,7 @@ struct ForwardArgs {
 
 struct BackwardArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 3-D maps over [B*H, N, d] bf16; Q, dO boxes of 64 rows, K, V of 128
+  CUtensorMap tm_dk, tm_dv;             // 3-D maps over dK, dV [B*H, N, d] fp32, box {32, 128, 1}, 128B swizzle
   const void* o;                        // [B, H, N, d] bf16 or fp32
   const void* dout;                     // [B, H, N, d] bf16
   const float* lse;                     // [B, H, N]
