@@ -20,12 +20,13 @@
 //                                                 K=16 bias product)
 //       dV += P^T dO_i and dK += dS^T Q_i        (TS MMA, A = P^T / dS^T in TMEM)
 //       dQ_i^T = K^T dS_i^T                      (SS MMA, M=d, N=64, dS from smem)
-//   warp 16 loads (TMA), warp 17 issues MMAs, warps 0-7 (thread = key, two
-//   warpgroups by query half) turn S^T, dP^T into P^T, dS^T, warps 8-15 (thread =
-//   feature) add dQ_i^T into dQ with fp32 reductions in L2.  S^T/dP^T are
-//   double-buffered in TMEM so the tensor core computes step n+1 while step n's
-//   elementwise work runs; dQ^T of step n lands in the dP^T buffer that dS^T of
-//   step n has just left.
+//   warp 16 loads (TMA), warp 17 issues MMAs, warp 18 waits on the mbarriers the
+//   issuer depends on and hands each completion to it through a hardware named
+//   barrier, warps 0-7 (thread = key, two warpgroups by query half) turn S^T into
+//   P^T and then dP^T into dS^T, warps 8-15 (thread = feature) add dQ_i^T into dQ
+//   with fp32 reductions in L2.  S^T/dP^T are double-buffered in TMEM so the tensor
+//   core computes step n+1 while step n's elementwise work runs; dQ^T of step n
+//   lands in the dP^T buffer that dS^T of step n has just left.
 // Tensor memory (512 columns): S^T[2] [0,64) [64,128), dP^T[2] [128,192)
 // [192,256), dV [256, 256+d), dK [256+d, 256+2d).
 #include <cuda_bf16.h>
@@ -46,11 +47,12 @@ constexpr int kBKV = 128;  // keys per CTA
 constexpr int kBQ = 64;    // queries per step
 // Warps 0-7: P^T / dS^T and warps 8-15: dQ writers (each two warpgroups, one per
 // half of the step's 64 query columns); warp 16: TMA producer; warp 17: MMA
-// issuer; warps 18-19 only lend their registers.
+// issuer; warp 18: the issuer's waits; warp 19 only lends its registers.
 constexpr int kBwdThreads = 640;
 constexpr int kWriterWarp0 = 8;
 constexpr int kProducerWarp = 16;
 constexpr int kMmaWarp = 17;
+constexpr int kWaitWarp = 18;
 // Register split (setmaxnreg) by warpgroup: each P/dS thread holds two 32-column
 // TMEM rows, each dQ writer one 32-column row, the producer / MMA warps little.
 // The sum stays within the CTA's launch allocation; the launcher checks it.
@@ -79,7 +81,7 @@ struct BwdCfg {
 struct BwdShared {
   uint64_t kv_full;
   uint64_t q_full[4], q_empty[4];
-  uint64_t sdp_full[2], p_full[2], dq_full[2], dq_empty[2], ds_empty[2];
+  uint64_t s_full[2], dp_full[2], p_full[2], ds_full[2], dq_full[2], dq_empty[2], ds_empty[2];
   uint64_t dkdv_full;
   uint64_t drain;
   uint32_t tmem_base;
@@ -101,6 +103,23 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
 
 // Named barrier over the 256 P/dS threads.
 __device__ __forceinline__ void compute_bar_sync() { asm volatile("barrier.cta.sync 2, 256;" ::: "memory"); }
+
+// Rendezvous of the MMA issuer and its waiting warp (named barrier 3, 64 threads),
+// returning the AND of both warps' flags.  A wait on an mbarrier is a shared-memory
+// access, which takes a few hundred cycles while the tensor core streams its
+// operands from shared memory; the waiting warp absorbs that latency while the
+// issuer is still queueing earlier products, and the hand-off itself is a hardware
+// barrier.  Both warps take the same sequence of rendezvous and leave their loops
+// on the same (shared) outcome, so neither can be left waiting.
+__device__ __forceinline__ bool issuer_rendezvous(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, 3, 64, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(ok))
+      : "memory");
+  return r != 0;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_constant__ BackwardArgs a) {
@@ -144,8 +163,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       mbar_init(&sh.q_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&sh.sdp_full[b], 1);
+      mbar_init(&sh.s_full[b], 1);
+      mbar_init(&sh.dp_full[b], 1);
       mbar_init(&sh.p_full[b], 256);
+      mbar_init(&sh.ds_full[b], 256);
       mbar_init(&sh.dq_full[b], 1);
       mbar_init(&sh.dq_empty[b], 256);
       mbar_init(&sh.ds_empty[b], 1);
@@ -222,55 +243,72 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         const uint64_t dDS_mn = sdesc_sw128(smem_u32(sDS), kBKV * 128, 1024);// dS buffer 0, MN-major (B of dQ^T)
         const uint64_t dOnes = sdesc_k16_noswizzle(smem_u32(sOnes));        // A of the bias products
         const uint64_t dBias = sdesc_k16_noswizzle(smem_u32(sBias));        // bias tiles, stage 0
-        bool ok = warp_wait(&sh.kv_full, 0, &sh.abort, &g_bwd_status);
-        // S^T(n) and dP^T(n) into buffer n & 1.  The S^T buffer's previous user (P^T of
-        // step n - 2, read by dV) is done by issue order; the dP^T buffer also held
-        // dQ^T of step n - 2, so the dQ writers must have drained it first.  S^T goes
-        // first so that its products cover that hand-off.  Each accumulator starts
-        // from its bias (one K = 16 product: ones x the three bf16 terms), so it ends
-        // holding S^T - LSE/scale and dP^T - D.
-        auto issue_sdp = [&](int n) -> bool {
-          const int s = n % C::kStages, b = n & 1;
-          if (!warp_wait(&sh.q_full[s], (n / C::kStages) & 1, &sh.abort, &g_bwd_status)) return false;
-          tc_fence_after();
-          const uint64_t q_d = desc_add(dQ_k, s * C::kQBytes), do_d = desc_add(dDO_k, s * C::kQBytes);
-          const uint32_t s_tm = tmem + b * kBQ;
-          const uint64_t bias_d = desc_add(dBias, s * C::kBiasBytes);
-          umma_ss(s_tm, dOnes, bias_d, kIdSdP, 0u, leader);
+        // Per step n the products go in the order S^T(n+1), dV(n), dP^T(n+1), dK(n),
+        // dQ^T(n), each after a rendezvous with the waiting warp (warp 18) that covers
+        // what it reads or overwrites:
+        //   S^T(n+1)  Q(n+1) loaded; its buffer's previous user, dV(n-1), came earlier;
+        //   dV(n)     P^T(n) in TMEM;
+        //   dP^T(n+1) the dQ writers have read dQ^T(n-1) from the same buffer;
+        //   dK(n), dQ^T(n)  dS^T(n) in TMEM and in shared memory.
+        // Each accumulator of S^T / dP^T starts from its bias (one K = 16 product: ones
+        // x the three bf16 terms), so it ends holding S^T - LSE/scale and dP^T - D.
+        auto issue_s = [&](int n) {
+          const int s = n % C::kStages;
+          const uint64_t q_d = desc_add(dQ_k, s * C::kQBytes);
+          const uint32_t s_tm = tmem + (n & 1) * kBQ;
+          umma_ss(s_tm, dOnes, desc_add(dBias, s * C::kBiasBytes), kIdSdP, 0u, leader);
   #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             umma_ss(s_tm, desc_add(dK_k, (kk >> 2) * (kBKV * 128) + (kk & 3) * 32),
                     desc_add(q_d, (kk >> 2) * (kBQ * 128) + (kk & 3) * 32), kIdSdP, 1u, leader);
-          if (n >= 2 && !warp_wait(&sh.dq_empty[b], ((n >> 1) - 1) & 1, &sh.abort, &g_bwd_status)) return false;
-          tc_fence_after();
-          umma_ss(s_tm + 128, dOnes, desc_add(bias_d, C::kBiasBytes / 2), kIdSdP, 0u, leader);
+          umma_commit(&sh.s_full[n & 1], leader);
+        };
+        auto issue_dp = [&](int n) {
+          const int s = n % C::kStages;
+          const uint64_t do_d = desc_add(dDO_k, s * C::kQBytes);
+          const uint32_t dp_tm = tmem + 128 + (n & 1) * kBQ;
+          umma_ss(dp_tm, dOnes, desc_add(dBias, s * C::kBiasBytes + C::kBiasBytes / 2), kIdSdP, 0u, leader);
   #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(s_tm + 128, desc_add(dV_k, (kk >> 2) * (kBKV * 128) + (kk & 3) * 32),
+            umma_ss(dp_tm, desc_add(dV_k, (kk >> 2) * (kBKV * 128) + (kk & 3) * 32),
                     desc_add(do_d, (kk >> 2) * (kBQ * 128) + (kk & 3) * 32), kIdSdP, 1u, leader);
-          umma_commit(&sh.sdp_full[b], leader);
-          return true;
+          umma_commit(&sh.dp_full[n & 1], leader);
         };
+        // P^T of query half h sits packed in columns [32h, 32h + 16) of the S^T buffer,
+        // dS^T likewise in the dP^T buffer.
+        auto pcol = [](int kk) { return (kk >> 1) * 32 + (kk & 1) * 8; };
+        bool ok = issuer_rendezvous(true);  // K, V and Q(0) loaded
         if (ok) {
           tc_fence_after();
-          ok = issue_sdp(0);
+          issue_s(0);
+          issue_dp(0);
         }
         for (int n = 0; ok && n < n_steps; ++n) {
           const int s = n % C::kStages, b = n & 1;
-          if (n + 1 < n_steps && !issue_sdp(n + 1)) break;
-          if (!warp_wait(&sh.p_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status)) break;
-          tc_fence_after();
-          const uint64_t q_d = desc_add(dQ_mn, s * C::kQBytes), do_d = desc_add(dDO_mn, s * C::kQBytes);
+          const bool next = n + 1 < n_steps;
           const uint32_t s_tm = tmem + b * kBQ;
           const uint32_t acc0 = n > 0 ? 1u : 0u;
-          // dV += P^T dO_i   (K = 64 queries; dO_i is the MN-major B operand).  P^T of
-          // query half h sits packed in columns [32h, 32h + 16) of the S^T buffer,
-          // dS^T likewise in the dP^T buffer.
-          auto pcol = [](int kk) { return (kk >> 1) * 32 + (kk & 1) * 8; };
+          if (next) {
+            if (!(ok = issuer_rendezvous(true))) break;
+            tc_fence_after();
+            issue_s(n + 1);
+          }
+          if (!(ok = issuer_rendezvous(true))) break;
+          tc_fence_after();
+          // dV += P^T dO_i   (K = 64 queries; dO_i is the MN-major B operand)
+          const uint64_t do_d = desc_add(dDO_mn, s * C::kQBytes);
   #pragma unroll
           for (int kk = 0; kk < kBQ / 16; ++kk)
             umma_ts(tmem + C::kDVCol, s_tm + pcol(kk), desc_add(do_d, kk * 16 * 128), kIdKV, kk > 0 ? 1u : acc0, leader);
+          if (next) {
+            if (!(ok = issuer_rendezvous(true))) break;
+            tc_fence_after();
+            issue_dp(n + 1);
+          }
+          if (!(ok = issuer_rendezvous(true))) break;
+          tc_fence_after();
           // dK += dS^T Q_i
+          const uint64_t q_d = desc_add(dQ_mn, s * C::kQBytes);
   #pragma unroll
           for (int kk = 0; kk < kBQ / 16; ++kk)
             umma_ts(tmem + C::kDKCol, s_tm + 128 + pcol(kk), desc_add(q_d, kk * 16 * 128), kIdKV, kk > 0 ? 1u : acc0, leader);
@@ -290,6 +328,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         mbar_wait_drain(&sh.drain, 0);
       }
       __syncwarp();
+    } else if (warp == kWaitWarp) {
+      // ------------------------------------------------------------ the issuer's waits
+      // The same sequence of rendezvous as the MMA issuer, each after the wait that
+      // the product issued next depends on.
+      bool ok = warp_wait(&sh.kv_full, 0, &sh.abort, &g_bwd_status) &&
+                warp_wait(&sh.q_full[0], 0, &sh.abort, &g_bwd_status);
+      ok = issuer_rendezvous(ok);
+      for (int n = 0; ok && n < n_steps; ++n) {
+        const int b = n & 1;
+        const bool next = n + 1 < n_steps;
+        if (next) {
+          const int s1 = (n + 1) % C::kStages;
+          if (!(ok = issuer_rendezvous(warp_wait(&sh.q_full[s1], ((n + 1) / C::kStages) & 1, &sh.abort, &g_bwd_status))))
+            break;
+        }
+        if (!(ok = issuer_rendezvous(warp_wait(&sh.p_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status)))) break;
+        if (next) {
+          // dP^T(n+1) overwrites dQ^T(n-1)
+          const bool w = n < 1 || warp_wait(&sh.dq_empty[(n - 1) & 1], ((n - 1) >> 1) & 1, &sh.abort, &g_bwd_status);
+          if (!(ok = issuer_rendezvous(w))) break;
+        }
+        if (!(ok = issuer_rendezvous(warp_wait(&sh.ds_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status)))) break;
+      }
     }
   } else if (warp < kWriterWarp0) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kComputeRegs));
@@ -305,11 +366,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     for (int n = 0; n < n_steps; ++n) {
       const int b = n & 1;
       const int q0 = (i_start + n) * kBQ;
-      if (!__all_sync(0xffffffffu, mbar_wait(&sh.sdp_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status))) {
+      // The dS tile of step n - 2 must have been read by dQ^T(n - 2) (checked first:
+      // it is long done, and the check's latency hides behind the wait for S^T).
+      if (n >= 2 && !__all_sync(0xffffffffu, mbar_wait(&sh.ds_empty[b], ((n >> 1) - 1) & 1, &sh.abort, &g_bwd_status))) {
         ok = false;
         break;
       }
-      if (n >= 2 && !__all_sync(0xffffffffu, mbar_wait(&sh.ds_empty[b], ((n >> 1) - 1) & 1, &sh.abort, &g_bwd_status))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sh.s_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status))) {
         ok = false;
         break;
       }
@@ -319,39 +382,56 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       const bool key_valid = key < a.N;
       const uint32_t s_tm = tmem_addr(tmem, lane_base, b * kBQ + 32 * h);
       const uint32_t dp_tm = tmem_addr(tmem, lane_base, 128 + b * kBQ + 32 * h);
-      uint8_t* ds_row = sDS + b * C::kDSBytes + (k >> 3) * 1024 + (k & 7) * 128;
-      // One TMEM round trip in (S^T and dP^T, 32 columns each) and one out.
-      uint32_t sv[32], dpv[32];
-      tmem_ld32x2(s_tm, dp_tm, sv, dpv);
-      uint32_t pk[16], dk[16];
+      // P^T first, while the tensor core still computes dP^T.  S^T arrives holding
+      // S^T - LSE/scale (the bias came with the product).
+      uint32_t sv[32];
+      tmem_ld32(s_tm, sv);
+      float p[32];
+      uint32_t pk[16];
       const float2 sl2x2 = make_float2(sl2, sl2);
-      // sv holds S^T - LSE/scale, dpv holds dP^T - D (the biases came with the products).
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
         const float2 arg = __fmul2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2x2);
-        float p0 = ex2(arg.x), p1 = ex2(arg.y);
+        p[e] = ex2(arg.x);
+        p[e + 1] = ex2(arg.y);
         if (need_mask) {
           const int qe = q0 + 32 * h + e;
-          if (!key_valid || qe < first_visible_q) p0 = 0.f;
-          if (!key_valid || qe + 1 < first_visible_q) p1 = 0.f;
+          if (!key_valid || qe < first_visible_q) p[e] = 0.f;
+          if (!key_valid || qe + 1 < first_visible_q) p[e + 1] = 0.f;
         }
+        pk[e / 2] = pack_bf16(p[e], p[e + 1]);
+      }
+      // P^T packed (queries 2c, 2c+1 in column c) over the first 16 of this half's 32
+      // columns, which this thread has already read.
+      tmem_st16(s_tm, pk);
+      tc_fence_before();
+      mbar_arrive(&sh.p_full[b]);
+      if (!__all_sync(0xffffffffu, mbar_wait(&sh.dp_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // dS^T = P^T * (dP^T - D); dP^T arrives holding dP^T - D.
+      uint32_t dpv[32];
+      tmem_ld32(dp_tm, dpv);
+      uint32_t dk[16];
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
         const float2 ds2 =
-            __fmul2_rn(make_float2(p0, p1), make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])));
-        pk[e / 2] = pack_bf16(p0, p1);
+            __fmul2_rn(make_float2(p[e], p[e + 1]), make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])));
         dk[e / 2] = pack_bf16(ds2.x, ds2.y);
       }
       // dS^T row of this key into the MN-major, 128B-swizzled dS tile:
       // 16-byte piece p (queries 8p..8p+7) of row k sits at ((p ^ (k & 7)) * 16).
+      uint8_t* ds_row = sDS + b * C::kDSBytes + (k >> 3) * 1024 + (k & 7) * 128;
 #pragma unroll
       for (int piece = 0; piece < 4; ++piece)
         *reinterpret_cast<uint4*>(ds_row + (((4 * h + piece) ^ (k & 7)) << 4)) =
             make_uint4(dk[4 * piece], dk[4 * piece + 1], dk[4 * piece + 2], dk[4 * piece + 3]);
-      // P^T and dS^T packed (queries 2c, 2c+1 in column c) over the first 16 of this
-      // half's 32 columns, which this thread has already read.
-      tmem_st16x2(s_tm, pk, dp_tm, dk);
+      tmem_st16(dp_tm, dk);
       tc_fence_before();
       fence_proxy_async_smem();
-      mbar_arrive(&sh.p_full[b]);
+      mbar_arrive(&sh.ds_full[b]);
     }
     // ------------------------------------------------------------ dK, dV epilogue
     // Once the last products are done, the Q/dO/dS buffers are free: dK and dV are
