@@ -111,15 +111,7 @@ __device__ __forceinline__ void compute_bar_sync() { asm volatile("barrier.cta.s
 // issuer is still queueing earlier products, and the hand-off itself is a hardware
 // barrier.  Both warps take the same sequence of rendezvous and leave their loops
 // on the same (shared) outcome, so neither can be left waiting.
-__device__ __forceinline__ bool issuer_rendezvous(bool ok) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, 3, 64, q;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(ok))
-      : "memory");
-  return r != 0;
-}
+__device__ __forceinline__ bool issuer_rendezvous(bool ok) { return bar_and(3, 64, ok); }
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_constant__ BackwardArgs a) {
@@ -480,7 +472,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     // lanes cover 128 contiguous bytes of the dQ row.
     const int half = (warp - kWriterWarp0) >> 2;  // query columns [32*half, 32*half + 32)
     const int lane_base = (warp & 3) * 32;
-    const int c = lane_base + lane;               // feature index == TMEM lane of dQ^T
     const bool has_rows = lane_base < D;          // for d = 64, lanes 64..127 hold no feature
     griddep_wait();  // dQ is zeroed by the preprocess kernel, which may still be running
     for (int n = 0; n < n_steps; ++n) {
@@ -493,11 +484,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       tc_fence_before();
       mbar_arrive(&sh.dq_empty[b]);
       if (has_rows) {
-        float* dst = a.dq + (static_cast<size_t>(bh) * a.N + q0) * D + c;
+        // 4 x 4 transposes within each group of four lanes (two shuffle rounds per
+        // block of four queries): lane 4g + i ends up with features 4g .. 4g + 3 of
+        // queries 4k + i, which leave as 16-byte vector reductions.  One warp
+        // instruction then covers four whole 128-byte row segments, a quarter of the
+        // instructions of one reduction per feature.
+        const int i4 = lane & 3;
+        float* dst = a.dq + (static_cast<size_t>(bh) * a.N + q0 + i4) * D + lane_base + 4 * (lane >> 2);
         const int rows = min(32, a.N - q0);
 #pragma unroll
-        for (int q = 0; q < 32; ++q)
-          if (q < rows) atomicAdd(dst + static_cast<size_t>(q) * D, __uint_as_float(v[q]) * a.scale);
+        for (int kq = 0; kq < 8; ++kq) {
+          const float x0 = __uint_as_float(v[4 * kq]) * a.scale, x1 = __uint_as_float(v[4 * kq + 1]) * a.scale;
+          const float x2 = __uint_as_float(v[4 * kq + 2]) * a.scale, x3 = __uint_as_float(v[4 * kq + 3]) * a.scale;
+          // Round 1 (lanes i, i ^ 1): even lanes keep queries 0 and 2, odd lanes 1 and 3,
+          // each for both features of the pair.
+          const bool odd = i4 & 1;
+          const float r0 = __shfl_xor_sync(0xffffffffu, odd ? x0 : x1, 1);
+          const float r1 = __shfl_xor_sync(0xffffffffu, odd ? x2 : x3, 1);
+          const float a0 = odd ? r0 : x0, a1 = odd ? x1 : r0, a2 = odd ? r1 : x2, a3 = odd ? x3 : r1;
+          // Round 2 (lanes i, i ^ 2): exchange the other feature pair.
+          const bool hi = i4 & 2;
+          const float t0 = __shfl_xor_sync(0xffffffffu, hi ? a0 : a2, 2);
+          const float t1 = __shfl_xor_sync(0xffffffffu, hi ? a1 : a3, 2);
+          const float y0 = hi ? t0 : a0, y1 = hi ? t1 : a1, y2 = hi ? a2 : t0, y3 = hi ? a3 : t1;
+          if (4 * kq + i4 < rows)
+            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + static_cast<size_t>(4 * kq) * D),
+                         "f"(y0), "f"(y1), "f"(y2), "f"(y3)
+                         : "memory");
+        }
       }
     }
   }

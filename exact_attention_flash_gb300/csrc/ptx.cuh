@@ -113,6 +113,18 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
   return true;
 }
 
+// Rendezvous of whole warps on named barrier `id` (`count` threads in all), returning
+// the AND of every participant's flag.  A hardware barrier: no shared-memory access.
+__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t count, bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %3, 0;\n bar.red.and.pred p, %1, %2, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"(id), "r"(count), "r"(static_cast<uint32_t>(ok))
+      : "memory");
+  return r != 0;
+}
+
 // ---------------------------------------------------------------- dependent launches
 // A kernel launched as a programmatic dependent of the previous one on its stream
 // may start before that one ends; griddep_wait blocks until the previous kernel has
