@@ -14,9 +14,11 @@ Sources (web pages on exact tiled attention; cited by title and section):
 
 * "attention_kernels.py" (CMU 15-779, lecture 5): section 1 ``SoftmaxState`` /
   ``merge_states`` / ``state_of_scores``; section 2 ``_scale``, ``_mask`` and
-  ``standard_attention``; section 4 ``flash_backward`` (its docstring derives
-  dS = P * (dP - D) from the softmax Jacobian diag(p) - p p^T); section 5
-  ``flash_decode``.
+  ``standard_attention``; section 3 ``flash_forward`` (the block-wise loop and
+  its ``stats`` counters); section 4 ``flash_backward`` (its docstring derives
+  dS = P * (dP - D) from the softmax Jacobian diag(p) - p p^T, and its
+  "dq_atomic_adds" counter); section 5 ``flash_decode``; section 6
+  ``io_flash``.
 * "lab.py" (hs-black, flash-attention post): ``dense``, ``tiled`` (row-wise
   online softmax returning the log-sum-exp) and ``backward`` (row-wise tiled
   gradient).
@@ -30,10 +32,13 @@ scores giving the mean of V, N=1 and first-causal-row special cases,
 ``scipy.special.logsumexp`` / ``softmax`` on the dense path, block-size
 invariance of the row-wise tiled path against the dense path (uneven last
 tiles included), finiteness at x100 logits, central finite differences and
-float64 autograd for both gradient paths, gradient invariants, and the
+float64 autograd for both gradient paths, gradient invariants, the
 algebraic laws of ``merge_states`` (identity, commutativity, associativity)
-with split decoding equal to dense attention for every split count.  No
-function here is "parity unpinned".
+with split decoding equal to dense attention for every split count, and for
+the block-wise loop: equality with the dense path for even and uneven blocks,
+its counters against closed forms and an element-wise brute force, and
+``io_flash`` against hand-computed values.  No function here is "parity
+unpinned".
 """
 from __future__ import annotations
 
@@ -235,6 +240,115 @@ def attention_tiled_rowwise_backward(q, k, v, out, lse, do, block, scale=None, c
             dk[start:stop] += np.outer(ds, q[i]) * sc
             dv[start:stop] += np.outer(p, do[i])
     return dq, dk, dv
+
+
+# --------------------------------------------------------------------------
+# Block-wise loop with the page's counters ("attention_kernels.py" §3, §4, §6)
+# --------------------------------------------------------------------------
+def _bump(stats, key, n):
+    if stats is not None:
+        stats[key] = stats.get(key, 0) + int(n)
+
+
+def attention_flash_blocked(q, k, v, br, bc, scale=None, causal=False, stats=None, rescale_margin=0.0):
+    """Online softmax over blocks: query blocks of ``br`` rows against key blocks of ``bc`` keys.
+
+    Query blocks outer, key blocks inner.  Under ``causal`` a key block whose first
+    key lies after the query block's last row (j0 > i1 - 1) is skipped whole; the
+    other blocks mask keys after each row to -inf.  Per computed block, with s the
+    block's scores: m_new = max(m, rowmax s), alpha = exp(m - m_new) (0 while m is
+    still -inf), p = exp(s - m_new), l = alpha l + rowsum p, acc = alpha acc + p V_j,
+    m = m_new.  Finally O_i = acc / l and L_i = m + log l.  Blocks may be uneven
+    at the end.
+
+    ``stats`` (a dict) receives the page's counters: "tiles" (blocks computed),
+    "skipped" (blocks skipped under causality) and "rescales" (rows of a computed
+    block whose running max grew from a finite value).  ``rescale_margin`` is not
+    on the page (default 0): a growth counts only when m_new > m + margin, so that
+    a test can bracket a count taken in another precision.
+    Source: "attention_kernels.py", section 3 ``flash_forward``.  Single head:
+    q (Nq, d), k (Nk, d), v (Nk, dv).
+    """
+    if br < 1 or bc < 1:
+        raise ValueError("block sizes must be >= 1")
+    q, k, v = _as_f64(q, k, v)
+    sc = default_scale(q.shape[1], scale)
+    nq, nk = q.shape[0], k.shape[0]
+    out = np.empty((nq, v.shape[1]))
+    lse = np.empty(nq)
+    for i0 in range(0, nq, br):
+        i1 = min(i0 + br, nq)
+        m = np.full(i1 - i0, NEG_INF)
+        l = np.zeros(i1 - i0)
+        acc = np.zeros((i1 - i0, v.shape[1]))
+        for j0 in range(0, nk, bc):
+            j1 = min(j0 + bc, nk)
+            if causal and j0 > i1 - 1:
+                _bump(stats, "skipped", 1)
+                continue
+            s = (q[i0:i1] @ k[j0:j1].T) * sc
+            if causal:
+                s = np.where(causal_mask(i0, i1 - i0, j1 - j0, k_start=j0), NEG_INF, s)
+            m_new = np.maximum(m, s.max(axis=1))
+            finite = np.isfinite(m)
+            alpha = np.where(finite, np.exp(np.where(finite, m, 0.0) - np.where(finite, m_new, 0.0)), 0.0)
+            p = np.exp(s - np.where(np.isfinite(m_new), m_new, 0.0)[:, None])
+            l = l * alpha + p.sum(axis=1)
+            acc = acc * alpha[:, None] + p @ v[j0:j1]
+            _bump(stats, "tiles", 1)
+            _bump(stats, "rescales", np.count_nonzero(finite & (m_new > np.where(finite, m, 0.0) + rescale_margin)))
+            m = m_new
+        out[i0:i1] = acc / l[:, None]
+        lse[i0:i1] = m + np.log(l)
+    return out, lse
+
+
+def attention_flash_blocked_backward(q, k, v, out, lse, do, br, bc, scale=None, causal=False, stats=None):
+    """Recompute backward over blocks: key blocks outer, query blocks inner.
+
+    D = rowsum(dO * O).  For key block j and query block i (skipped whole under
+    causality when j0 > i1 - 1): P = exp(S - L_i) with future keys masked,
+    dV_j += P^T dO_i, dP = dO_i V_j^T, dS = P * (dP - D_i), dQ_i += dS K_j * scale,
+    dK_j += dS^T Q_i * scale.  ``stats`` receives the page's "dq_atomic_adds":
+    (i1 - i0) * d per computed block, the dQ elements a GPU adds atomically.
+    Source: "attention_kernels.py", section 4 ``flash_backward``.  Single head.
+    """
+    if br < 1 or bc < 1:
+        raise ValueError("block sizes must be >= 1")
+    q, k, v, out, lse, do = _as_f64(q, k, v, out, lse, do)
+    sc = default_scale(q.shape[1], scale)
+    nq, nk = q.shape[0], k.shape[0]
+    row_dot = (do * out).sum(axis=1)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for j0 in range(0, nk, bc):
+        j1 = min(j0 + bc, nk)
+        for i0 in range(0, nq, br):
+            i1 = min(i0 + br, nq)
+            if causal and j0 > i1 - 1:
+                continue
+            s = (q[i0:i1] @ k[j0:j1].T) * sc
+            if causal:
+                s = np.where(causal_mask(i0, i1 - i0, j1 - j0, k_start=j0), NEG_INF, s)
+            p = np.exp(s - lse[i0:i1, None])
+            dv[j0:j1] += p.T @ do[i0:i1]
+            dp = do[i0:i1] @ v[j0:j1].T
+            ds = p * (dp - row_dot[i0:i1, None])
+            dq[i0:i1] += (ds @ k[j0:j1]) * sc
+            dk[j0:j1] += (ds.T @ q[i0:i1]) * sc
+            _bump(stats, "dq_atomic_adds", (i1 - i0) * q.shape[1])
+    return dq, dk, dv
+
+
+def io_flash(n: int, d: int, br: int, kv_cached: bool = False) -> float:
+    """Elements the block-wise forward moves to and from device memory.
+
+    Q read once (N d), O written once (N d), L written (N); every query block reads
+    all of K and V (2 N d each time, ceil(N / br) times), or once when they stay
+    in cache (``kv_cached``), leaving 4 N d + N.
+    Source: "attention_kernels.py", section 6 ``io_flash``.
+    """
+    kv_reads = 2.0 * n * d * (1 if kv_cached else -(-n // br))
+    return 2.0 * n * d + kv_reads + n
 
 
 # --------------------------------------------------------------------------

@@ -9,6 +9,7 @@ import pytest
 import scipy.special
 
 from tests.golden.fixtures import load
+from tests.test_oracle_blocked import _block_any, _brute_rescales, _visible
 
 SRC = (Path(__file__).resolve().parent.parent / "oracle" / "attention.py").read_text()
 
@@ -60,6 +61,26 @@ def _pins_pass(o) -> bool:
             t_o, t_l = o.attention_tiled_rowwise(q, k, v, 2, causal=causal)
             for a, b in zip(o.attention_tiled_rowwise_backward(q, k, v, t_o, t_l, do, 2, causal=causal), fd):
                 np.testing.assert_allclose(a, b, atol=2e-8, rtol=2e-6)
+        # the block-wise loop with its counters ("attention_kernels.py" sections 3, 4, 6)
+        qb, kb, vb, dob = (rng.normal(size=(11, 4)) for _ in range(4))
+        for causal in (False, True):
+            d_o, d_l = o.attention_dense(qb, kb, vb, causal=causal)
+            d_g = o.attention_dense_backward(qb, kb, vb, dob, causal=causal)
+            for br, bc in ((2, 3), (4, 2), (3, 3)):
+                st, sb = {}, {}
+                b_o, b_l = o.attention_flash_blocked(qb, kb, vb, br, bc, causal=causal, stats=st)
+                np.testing.assert_allclose(b_o, d_o, atol=1e-12)
+                np.testing.assert_allclose(b_l, d_l, atol=1e-12)
+                b_g = o.attention_flash_blocked_backward(qb, kb, vb, d_o, d_l, dob, br, bc, causal=causal, stats=sb)
+                for a, b in zip(b_g, d_g):
+                    np.testing.assert_allclose(a, b, atol=1e-11)
+                computed = _block_any(_visible(11, causal), br, bc)
+                assert st.get("tiles", 0) == int(computed.sum())
+                assert st.get("skipped", 0) == int(computed.size - computed.sum())
+                assert st.get("rescales", 0) == _brute_rescales(qb, kb, br, bc, causal)
+                rows = np.array([min(br, 11 - a * br) for a in range(computed.shape[0])])
+                assert sb["dq_atomic_adds"] == int((computed.sum(axis=1) * rows).sum()) * 4
+        assert o.io_flash(8, 2, 4) == 104 and o.io_flash(8, 2, 4, kv_cached=True) == 72
         assert o.split_bounds(10, 4) == [0, 2, 5, 8, 10]
         qd, kd, vd = rng.normal(size=(1, 8)), rng.normal(size=(13, 8)), rng.normal(size=(13, 8))
         ref_o, ref_l = o.attention_dense(qd, kd, vd)
@@ -90,6 +111,12 @@ MUTATIONS = [
     ("merge uses wrong rebase", "a.l * ca + b.l * cb", "a.l * ca + b.l * ca"),
     ("floor split bounds", "round(Fraction(nk * s, n_split))", "int(Fraction(nk * s, n_split))"),
     ("decode drops last segment", "for part in parts[1:]:", "for part in parts[1:-1]:"),
+    ("blocked: no accumulator rescale", "acc = acc * alpha[:, None] + p @ v[j0:j1]", "acc = acc + p @ v[j0:j1]"),
+    ("blocked: causal skip one block late", "if causal and j0 > i1 - 1:\n                _bump", "if causal and j0 > i1:\n                _bump"),
+    ("blocked: rescales counted from -inf", "np.count_nonzero(finite & (m_new >", "np.count_nonzero((m_new >"),
+    ("blocked backward: D term dropped", "ds = p * (dp - row_dot[i0:i1, None])", "ds = p * dp"),
+    ("blocked backward: dq adds miss rows", "(i1 - i0) * q.shape[1])", "q.shape[1])"),
+    ("io_flash: K and V always cached", "(1 if kv_cached else -(-n // br))", "1"),
 ]
 
 
