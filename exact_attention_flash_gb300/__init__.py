@@ -12,7 +12,12 @@ from . import _lib
 from ._lib import FAError
 
 __all__ = ["fa_forward", "fa_backward", "fa_decode", "fa_device_status", "FAError", "backward_workspace_bytes",
-           "decode_workspace_bytes"]
+           "decode_workspace_bytes", "fa_set_stats", "stats_counters", "STATS_FIELDS"]
+
+import contextlib
+
+# Order of the counters behind fa_set_stats ("attention_kernels.py" sections 3-4, ``stats``).
+STATS_FIELDS = ("tiles", "skipped", "rescales", "dq_atomic_adds")
 
 
 def _stream_ptr(stream) -> int:
@@ -115,3 +120,30 @@ def fa_decode(q, k, v, n_split, scale=None, return_partials=False, workspace=Non
 def fa_device_status(stream=None) -> int:
     """Synchronise and return (and clear) the kernels' device status as an fa_status code."""
     return int(_lib.load().fa_device_status(_stream_ptr(stream)))
+
+
+def fa_set_stats(counters=None) -> None:
+    """Count the page's ``stats`` for the fa_forward / fa_backward calls this host thread makes.
+
+    ``counters``: a CUDA int64 tensor of 4 elements (zeroed by the caller), which
+    the kernels add into in the order of ``STATS_FIELDS``; None stops counting.
+    See ``fa_set_stats`` in ``include/fa_gb300.h`` for what each counter holds.
+    """
+    if counters is None:
+        ptr = None
+    else:
+        if not counters.is_cuda or counters.dtype != torch.int64 or counters.numel() != 4 or not counters.is_contiguous():
+            raise ValueError("counters must be a contiguous CUDA int64 tensor of 4 elements")
+        ptr = counters.data_ptr()
+    _lib.check("fa_set_stats", _lib.load().fa_set_stats(ptr))
+
+
+@contextlib.contextmanager
+def stats_counters(device=None):
+    """Zeroed counters set for the calls inside the ``with`` block; yields the tensor."""
+    c = torch.zeros(4, dtype=torch.int64, device=device or "cuda")
+    fa_set_stats(c)
+    try:
+        yield c
+    finally:
+        fa_set_stats(None)

@@ -37,6 +37,7 @@ SIGNATURES = {
     "fa_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _Z, _P]),
     "fa_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
     "fa_device_status": (_I, [_P]),
+    "fa_set_stats": (_I, [_P]),
     "fa_debug_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
 }
 

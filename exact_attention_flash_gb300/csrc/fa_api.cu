@@ -74,6 +74,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Counters set by fa_set_stats for the calling host thread's calls (null: none).
+thread_local unsigned long long* t_stats = nullptr;
+
 }  // namespace
 
 extern "C" {
@@ -115,6 +118,7 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, fa_dt
   a.head_group = fa::head_group_for(a.causal, 2ll * N * d * 2, B * H);  // K and V of a head, bf16
   a.o_f32 = (o_dtype == FA_F32) ? 1 : 0;
   a.precise = precise ? 1 : 0;
+  a.stats = t_stats;
   return fa::launch_forward(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -164,6 +168,7 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
   a.causal = causal ? 1 : 0;
   a.head_group = fa::head_group_for(a.causal, 2ll * N * d * 2 + static_cast<long long>(N) * d * 4, B * H);  // Q, dO, dQ
   a.o_f32 = (o_dtype == FA_F32) ? 1 : 0;
+  a.stats = t_stats;
   const cudaError_t e = fa::launch_backward(a, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -217,6 +222,12 @@ fa_status fa_device_status(void* stream) {
   const unsigned all = f | b | dcd;
   if (all & 1u) return FA_ERR_TIMEOUT;
   if (all != 0u) return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+fa_status fa_set_stats(unsigned long long* counters) {
+  if ((reinterpret_cast<uintptr_t>(counters) & 7u) != 0) return FA_ERR_INVALID_ARG;
+  t_stats = counters;
   return FA_OK;
 }
 

@@ -474,6 +474,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     const int lane_base = (warp & 3) * 32;
     const bool has_rows = lane_base < D;          // for d = 64, lanes 64..127 hold no feature
     griddep_wait();  // dQ is zeroed by the preprocess kernel, which may still be running
+    unsigned n_added = 0;  // dQ elements this thread added (fa_set_stats counters)
     for (int n = 0; n < n_steps; ++n) {
       const int b = n & 1;
       const int q0 = (i_start + n) * kBQ + 32 * half;
@@ -507,12 +508,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
           const float t0 = __shfl_xor_sync(0xffffffffu, hi ? a0 : a2, 2);
           const float t1 = __shfl_xor_sync(0xffffffffu, hi ? a1 : a3, 2);
           const float y0 = hi ? t0 : a0, y1 = hi ? t1 : a1, y2 = hi ? a2 : t0, y3 = hi ? a3 : t1;
-          if (4 * kq + i4 < rows)
+          if (4 * kq + i4 < rows) {
             asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + static_cast<size_t>(4 * kq) * D),
                          "f"(y0), "f"(y1), "f"(y2), "f"(y3)
                          : "memory");
+            n_added += 4u;
+          }
         }
       }
+    }
+    if (a.stats != nullptr) {  // one addition per warp and CTA
+      const unsigned added = __reduce_add_sync(0xffffffffu, n_added);
+      if (lane == 0 && added != 0u) atomicAdd(a.stats + 3, static_cast<unsigned long long>(added));
     }
   }
 

@@ -279,6 +279,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         };
         int g = 0;                  // K/V tiles consumed (the ring position)
         int step[kTiles] = {0, 0};  // per-tile steps before the current item
+        // fa_set_stats counters: S products of query tiles that start before N, and
+        // the key tiles causality skipped for them.
+        unsigned n_tiles = 0, n_skipped = 0;
+        const int n_kv_total = (a.N + kBN - 1) / kBN;
         bool ok = true;
         for (int it = 0; ok; ++it) {
           const int r = it % kItemRing;
@@ -287,6 +291,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           mbar_arrive(&bars.item_empty[r]);
           if (item >= n_items) break;
           const FwdItem w = fwd_item(a, item);
+#pragma unroll
+          for (int t = 0; t < kTiles; ++t)
+            if (w.q_row0 + t * kBM < a.N) {
+              n_tiles += w.n_kv[t];
+              n_skipped += n_kv_total - w.n_kv[t];
+            }
           const int s0 = g % C::kStages;
           ok = warp_wait(&bars.k_full[s0], (g / C::kStages) & 1, &bars.abort, &g_fwd_status);
           for (int t = 0; ok && t < kTiles; ++t) {
@@ -335,6 +345,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         // Drain: all MMAs complete before tensor memory is released.
         umma_commit(&bars.drain, leader);
         mbar_wait_drain(&bars.drain, 0);
+        if (a.stats != nullptr && lane == 0) {
+          if (n_tiles != 0u) atomicAdd(a.stats + 0, static_cast<unsigned long long>(n_tiles));
+          if (n_skipped != 0u) atomicAdd(a.stats + 1, static_cast<unsigned long long>(n_skipped));
+        }
       }
       __syncwarp();
     }
@@ -348,6 +362,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     const uint32_t o_tm = tmem_addr(tmem, lane_base, C::kOCol + t * D);
     const float sl2 = a.scale_log2;
     int step = 0;  // this tile's steps across items (the S and P barriers' phase)
+    unsigned n_rescales = 0;  // running-max growths of this row (fa_set_stats counters)
     bool ok = true;
     for (int it = 0; ok; ++it) {
     const int ring = it % kItemRing;
@@ -359,6 +374,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     const FwdItem w = fwd_item(a, item);
     const int q_row0 = w.q_row0, bh = w.bh;
     const int row = q_row0 + t * kBM + r;
+    float mx_seen = -INFINITY;  // true running max of the raw scores (counters only)
     float m_run = -INFINITY;  // reference max (scaled, log2 units)
     float l_run = 0.f;  // sum of p: the log-sum-exp
     float l_hat = 0.f;  // sum of the bf16-rounded p that enter P V: the normaliser of O
@@ -397,6 +413,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         mx8[c] = fmaxf(v, x[16 * c + 15]);
       }
       const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+      n_rescales += (row < a.N && mx > mx_seen && mx_seen != -INFINITY) ? 1u : 0u;
+      mx_seen = fmaxf(mx_seen, mx);
       const float m_tile = mx * sl2;
       float m_use = m_run;
       float alpha = 1.f;
@@ -517,6 +535,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       }
       if (row < a.N) a.lse[static_cast<size_t>(bh) * a.N + row] = (m_run + __log2f(l_run)) * kLn2;
     }
+    }
+    if (a.stats != nullptr) {  // fa_set_stats counters: one addition per warp and CTA
+      const unsigned resc = __reduce_add_sync(0xffffffffu, n_rescales);
+      if (lane == 0 && resc != 0u) atomicAdd(a.stats + 2, static_cast<unsigned long long>(resc));
     }
   }
 

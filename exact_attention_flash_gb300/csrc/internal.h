@@ -19,6 +19,7 @@ struct ForwardArgs {
   int precise;                   // 1: P enters PV as a bf16 hi + lo pair (two MMAs)
   unsigned* sched;               // set by the launcher: {items claimed, CTAs finished}, zero between launches
   int head_group;                // heads interleaved in the work order (set by the API, see head_group_for)
+  unsigned long long* stats;     // optional counters [tiles, skipped, rescales, dq adds]; null: none
 };
 
 struct BackwardArgs {
@@ -39,6 +40,7 @@ struct BackwardArgs {
   int causal;
   int o_f32;
   int head_group;                       // heads interleaved in the grid order (set by the API, see head_group_for)
+  unsigned long long* stats;            // optional counters [tiles, skipped, rescales, dq adds]; null: none
 };
 
 // Heads whose blocks are interleaved in the work order.  Under causality a block's

@@ -160,6 +160,36 @@ fa_status fa_decode_noalloc(const void* q, const void* k, const void* v, float* 
 fa_status fa_device_status(void* stream);
 
 /*
+ * fa_set_stats — counters of the pages' ``stats`` dictionary, for debugging and
+ * tests.
+ *
+ * Defines: "attention_kernels.py" section 3 ``flash_forward`` (counters
+ * "tiles", "skipped", "rescales") and section 4 ``flash_backward``
+ * ("dq_atomic_adds").  While a buffer is set, every fa_forward and fa_backward
+ * call made from the calling host thread adds into it.  `counters` is device
+ * memory: 4 unsigned 64-bit words, zeroed by the caller, owned by the caller.
+ *   [0] tiles           (query tile of 128 rows, key tile of 128) pairs the
+ *                       forward computed; query tiles that start at or past N
+ *                       do not count.
+ *   [1] skipped         such pairs the forward skipped under causality (the key
+ *                       tile starts after the query tile's last row).
+ *   [2] rescales        (query row, computed key tile) pairs in which the row's
+ *                       running maximum score grew from a finite value; rows at
+ *                       or past N do not count.
+ *   [3] dq_atomic_adds  dQ elements the backward added: per computed (query
+ *                       block of 64 rows, key tile of 128) pair, its rows (fewer
+ *                       in a last, partial block) times d.
+ * Summed over batch and heads, these equal the page's counts for blocks
+ * Br = Bc = 128 (forward) and Br = 64, Bc = 128 (backward) times B * H, since the
+ * page counts each block pair once for all heads; "rescales" equals the page's
+ * count directly (the page sums it over all rows).  The kernels add each CTA's
+ * counts once, at its end, so counting costs next to nothing.  NULL (the
+ * default) stops counting.  Returns FA_OK; FA_ERR_INVALID_ARG if `counters` is
+ * not 8-byte aligned.
+ */
+fa_status fa_set_stats(unsigned long long* counters);
+
+/*
  * fa_debug_wait_timeout — test hook for the failure path: queues one CTA that
  * waits on a barrier nothing completes, with a limit of `limit_ns`
  * nanoseconds.  The kernel returns on its own; the next fa_device_status()

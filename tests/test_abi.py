@@ -82,6 +82,13 @@ def test_decode_rejects_bad_arguments(lib):
     assert lib.fa_debug_wait_timeout(0, None) == 1
 
 
+def test_set_stats_arguments(lib):
+    # the counters must be 8-byte aligned; NULL stops counting (nothing runs here)
+    assert lib.fa_set_stats(FAKE + 4) == 1
+    assert lib.fa_set_stats(FAKE) == 0
+    assert lib.fa_set_stats(None) == 0
+
+
 def test_python_layer_fails_loudly_without_library(monkeypatch, tmp_path):
     from exact_attention_flash_gb300 import _lib
 
