@@ -81,6 +81,18 @@ def _pins_pass(o) -> bool:
                 rows = np.array([min(br, 11 - a * br) for a in range(computed.shape[0])])
                 assert sb["dq_atomic_adds"] == int((computed.sum(axis=1) * rows).sum()) * 4
         assert o.io_flash(8, 2, 4) == 104 and o.io_flash(8, 2, 4, kv_cached=True) == 72
+        # a query block at the end of a square causal problem (general q_start)
+        qs_o, qs_l = o.attention_dense(qb[7:], kb, vb, causal=True, q_start=7)
+        sq_o, sq_l = o.attention_dense(qb, kb, vb, causal=True)
+        np.testing.assert_allclose(qs_o, sq_o[7:], atol=1e-13)
+        np.testing.assert_allclose(qs_l, sq_l[7:], atol=1e-13)
+        dob4 = np.zeros_like(dob)
+        dob4[7:] = dob[7:]
+        g_block = o.attention_dense_backward(qb[7:], kb, vb, dob[7:], causal=True, q_start=7)
+        g_square = o.attention_dense_backward(qb, kb, vb, dob4, causal=True)
+        np.testing.assert_allclose(g_block[0], g_square[0][7:], atol=1e-12)  # dQ of the block's rows
+        np.testing.assert_allclose(g_block[1], g_square[1], atol=1e-12)      # dK
+        np.testing.assert_allclose(g_block[2], g_square[2], atol=1e-12)      # dV
         assert o.split_bounds(10, 4) == [0, 2, 5, 8, 10]
         qd, kd, vd = rng.normal(size=(1, 8)), rng.normal(size=(13, 8)), rng.normal(size=(13, 8))
         ref_o, ref_l = o.attention_dense(qd, kd, vd)
@@ -117,6 +129,9 @@ MUTATIONS = [
     ("blocked backward: D term dropped", "ds = p * (dp - row_dot[i0:i1, None])", "ds = p * dp"),
     ("blocked backward: dq adds miss rows", "(i1 - i0) * q.shape[1])", "q.shape[1])"),
     ("io_flash: K and V always cached", "(1 if kv_cached else -(-n // br))", "1"),
+    ("mask ignores q_start", "qpos = np.arange(q_start, q_start + nq)[:, None]", "qpos = np.arange(0, nq)[:, None]"),
+    ("dense backward ignores q_start", "_, _, p = _dense_rows(q_rows, k[h], v[h], sc, causal, q_start + r0)",
+     "_, _, p = _dense_rows(q_rows, k[h], v[h], sc, causal, r0)"),
 ]
 
 
