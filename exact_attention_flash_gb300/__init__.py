@@ -36,55 +36,79 @@ def _scale_arg(scale):
     return 0.0 if scale is None else float(scale)
 
 
+def _check_out(name, t, shape, dtypes):
+    if not t.is_cuda or t.dtype not in dtypes or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be a contiguous CUDA tensor of shape {tuple(shape)} and dtype in {dtypes}")
+
+
 def fa_forward(q, k, v, causal=False, scale=None, out_dtype=torch.bfloat16, precise=False, out=None, lse=None,
-               stream=None):
-    """O, LSE = softmax(Q K^T * scale [causal]) V for [B, H, N, d] bf16 inputs."""
+               stream=None, q_start=0):
+    """O, LSE = softmax(Q K^T * scale [causal]) V.
+
+    q [B, H, Nq, d], k and v [B, H, Nk, d], bf16.  Query row i sits at position
+    q_start + i; with ``causal`` it sees the keys j <= q_start + i.  Nq = Nk with
+    q_start = 0 is ordinary self-attention.
+    """
     lib = _lib.load()
     _check_bf16("q", q)
-    B, H, N, d = q.shape
-    _check_bf16("k", k, q.shape)
-    _check_bf16("v", v, q.shape)
+    B, H, Nq, d = q.shape
+    if k.dim() != 4:
+        raise ValueError("k must be [B, H, Nk, d]")
+    Nk = k.shape[2]
+    _check_bf16("k", k, (B, H, Nk, d))
+    _check_bf16("v", v, (B, H, Nk, d))
     if out is None:
-        out = torch.empty((B, H, N, d), device=q.device, dtype=out_dtype)
+        out = torch.empty((B, H, Nq, d), device=q.device, dtype=out_dtype)
+    _check_out("out", out, (B, H, Nq, d), (torch.bfloat16, torch.float32))
     if lse is None:
-        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+        lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
+    _check_out("lse", lse, (B, H, Nq), (torch.float32,))
     o_code = _lib.FA_F32 if out.dtype == torch.float32 else _lib.FA_BF16
-    if out.dtype not in (torch.float32, torch.bfloat16):
-        raise ValueError("out dtype must be bf16 or fp32")
-    code = lib.fa_forward(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), o_code, lse.data_ptr(),
-                          B, H, N, d, _scale_arg(scale), int(bool(causal)), int(bool(precise)), _stream_ptr(stream))
-    _lib.check("fa_forward", code)
+    code = lib.fa_forward_qk(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), o_code, lse.data_ptr(),
+                             B, H, Nq, Nk, int(q_start), d, _scale_arg(scale), int(bool(causal)), int(bool(precise)),
+                             _stream_ptr(stream))
+    _lib.check("fa_forward_qk", code)
     return out, lse
 
 
 def backward_workspace_bytes(B, H, N, d) -> int:
+    """Workspace of fa_backward for N (= Nq) query rows."""
     return int(_lib.load().fa_backward_workspace_size(B, H, N, d))
 
 
 def fa_backward(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, dk=None, dv=None,
-                stream=None):
-    """dQ, dK, dV (fp32) of sum(O * dO) by recomputation from LSE."""
+                stream=None, q_start=0):
+    """dQ, dK, dV (fp32) of sum(O * dO) by recomputation from LSE.
+
+    Shapes as for :func:`fa_forward` (q, o, do [B, H, Nq, d]; k, v [B, H, Nk, d];
+    lse [B, H, Nq]); causal, scale and q_start must match the forward call.
+    """
     lib = _lib.load()
     _check_bf16("q", q)
-    B, H, N, d = q.shape
-    for name, t in (("k", k), ("v", v), ("do", do)):
-        _check_bf16(name, t, q.shape)
-    if o.dtype not in (torch.bfloat16, torch.float32) or not o.is_contiguous() or tuple(o.shape) != tuple(q.shape):
-        raise ValueError("o must be a contiguous bf16/fp32 tensor shaped like q")
-    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N):
-        raise ValueError("lse must be fp32 [B, H, N]")
-    nbytes = backward_workspace_bytes(B, H, N, d)
+    B, H, Nq, d = q.shape
+    if k.dim() != 4:
+        raise ValueError("k must be [B, H, Nk, d]")
+    Nk = k.shape[2]
+    _check_bf16("k", k, (B, H, Nk, d))
+    _check_bf16("v", v, (B, H, Nk, d))
+    _check_bf16("do", do, q.shape)
+    _check_out("o", o, q.shape, (torch.bfloat16, torch.float32))
+    _check_out("lse", lse, (B, H, Nq), (torch.float32,))
+    nbytes = backward_workspace_bytes(B, H, Nq, d)
     if workspace is None:
         workspace = torch.empty(nbytes, device=q.device, dtype=torch.uint8)
-    dq = torch.empty(q.shape, device=q.device, dtype=torch.float32) if dq is None else dq
-    dk = torch.empty(q.shape, device=q.device, dtype=torch.float32) if dk is None else dk
-    dv = torch.empty(q.shape, device=q.device, dtype=torch.float32) if dv is None else dv
+    dq = torch.empty((B, H, Nq, d), device=q.device, dtype=torch.float32) if dq is None else dq
+    dk = torch.empty((B, H, Nk, d), device=q.device, dtype=torch.float32) if dk is None else dk
+    dv = torch.empty((B, H, Nk, d), device=q.device, dtype=torch.float32) if dv is None else dv
+    _check_out("dq", dq, (B, H, Nq, d), (torch.float32,))
+    _check_out("dk", dk, (B, H, Nk, d), (torch.float32,))
+    _check_out("dv", dv, (B, H, Nk, d), (torch.float32,))
     o_code = _lib.FA_F32 if o.dtype == torch.float32 else _lib.FA_BF16
-    code = lib.fa_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), o_code, lse.data_ptr(),
-                           do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
-                           _scale_arg(scale), int(bool(causal)), workspace.data_ptr(), workspace.numel(),
-                           _stream_ptr(stream))
-    _lib.check("fa_backward", code)
+    code = lib.fa_backward_qk(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), o_code, lse.data_ptr(),
+                              do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, int(q_start), d,
+                              _scale_arg(scale), int(bool(causal)), workspace.data_ptr(), workspace.numel(),
+                              _stream_ptr(stream))
+    _lib.check("fa_backward_qk", code)
     return dq, dk, dv
 
 

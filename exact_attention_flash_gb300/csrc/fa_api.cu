@@ -68,6 +68,15 @@ fa_status check_common(int B, int H, int N, int d) {
   return FA_OK;
 }
 
+// Query and key lengths and the query offset: Nq, Nk >= 1, q_start >= 0, and the
+// last query position q_start + Nq - 1 inside int.
+fa_status check_lengths(int B, int H, int Nq, int Nk, int q_start, int d) {
+  fa_status st = check_common(B, H, Nq, d);
+  if (st != FA_OK) return st;
+  if (Nk < 1 || q_start < 0 || static_cast<long long>(q_start) + Nq > 0x7FFFFFFFLL) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
 float resolve_scale(float scale, int d) { return scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(d)); }
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -97,25 +106,33 @@ const char* fa_status_string(fa_status s) {
 
 fa_status fa_forward(const void* q, const void* k, const void* v, void* o, fa_dtype o_dtype, float* lse, int B,
                      int H, int N, int d, float scale, int causal, int precise, void* stream) {
+  return fa_forward_qk(q, k, v, o, o_dtype, lse, B, H, N, N, 0, d, scale, causal, precise, stream);
+}
+
+fa_status fa_forward_qk(const void* q, const void* k, const void* v, void* o, fa_dtype o_dtype, float* lse, int B,
+                        int H, int Nq, int Nk, int q_start, int d, float scale, int causal, int precise,
+                        void* stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
   if (o_dtype != FA_BF16 && o_dtype != FA_F32) return FA_ERR_INVALID_ARG;
-  fa_status st = check_common(B, H, N, d);
+  fa_status st = check_lengths(B, H, Nq, Nk, q_start, d);
   if (st != FA_OK) return st;
   fa::ForwardArgs a{};
   const int BH = B * H;
-  if ((st = make_row_tile_map(&a.tm_q, q, BH, N, d)) != FA_OK) return st;
-  if ((st = make_row_tile_map(&a.tm_k, k, BH, N, d)) != FA_OK) return st;
-  if ((st = make_row_tile_map(&a.tm_v, v, BH, N, d)) != FA_OK) return st;
+  if ((st = make_row_tile_map(&a.tm_q, q, BH, Nq, d)) != FA_OK) return st;
+  if ((st = make_row_tile_map(&a.tm_k, k, BH, Nk, d)) != FA_OK) return st;
+  if ((st = make_row_tile_map(&a.tm_v, v, BH, Nk, d)) != FA_OK) return st;
   a.o = o;
   a.lse = lse;
   a.B = B;
   a.H = H;
-  a.N = N;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.q_start = q_start;
   a.d = d;
   a.scale_log2 = resolve_scale(scale, d) * kLog2e;
   a.causal = causal ? 1 : 0;
-  a.head_group = fa::head_group_for(a.causal, 2ll * N * d * 2, B * H);  // K and V of a head, bf16
+  a.head_group = fa::head_group_for(a.causal, 2ll * Nk * d * 2, B * H);  // K and V of a head, bf16
   a.o_f32 = (o_dtype == FA_F32) ? 1 : 0;
   a.precise = precise ? 1 : 0;
   a.stats = t_stats;
@@ -134,39 +151,49 @@ size_t fa_backward_workspace_size(int B, int H, int N, int d) {
 fa_status fa_backward(const void* q, const void* k, const void* v, const void* o, fa_dtype o_dtype,
                       const float* lse, const void* dout, float* dq, float* dk, float* dv, int B, int H, int N, int d,
                       float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
+  return fa_backward_qk(q, k, v, o, o_dtype, lse, dout, dq, dk, dv, B, H, N, N, 0, d, scale, causal, workspace,
+                        workspace_bytes, stream);
+}
+
+fa_status fa_backward_qk(const void* q, const void* k, const void* v, const void* o, fa_dtype o_dtype,
+                         const float* lse, const void* dout, float* dq, float* dk, float* dv, int B, int H, int Nq,
+                         int Nk, int q_start, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
+                         void* stream) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
       !aligned16(dk) || !aligned16(dv))
     return FA_ERR_INVALID_ARG;
   if (o_dtype != FA_BF16 && o_dtype != FA_F32) return FA_ERR_INVALID_ARG;
-  fa_status st = check_common(B, H, N, d);
+  fa_status st = check_lengths(B, H, Nq, Nk, q_start, d);
   if (st != FA_OK) return st;
-  if (!workspace || !aligned16(workspace) || workspace_bytes < fa_backward_workspace_size(B, H, N, d))
+  if (!workspace || !aligned16(workspace) || workspace_bytes < fa_backward_workspace_size(B, H, Nq, d))
     return FA_ERR_WORKSPACE;
   fa::BackwardArgs a{};
   const int BH = B * H;
-  if ((st = make_row_tile_map(&a.tm_q, q, BH, N, d, 64)) != FA_OK) return st;
-  if ((st = make_row_tile_map(&a.tm_k, k, BH, N, d, 128)) != FA_OK) return st;
-  if ((st = make_row_tile_map(&a.tm_v, v, BH, N, d, 128)) != FA_OK) return st;
-  if ((st = make_row_tile_map(&a.tm_do, dout, BH, N, d, 64)) != FA_OK) return st;
-  if ((st = make_grad_store_map(&a.tm_dk, dk, BH, N, d)) != FA_OK) return st;
-  if ((st = make_grad_store_map(&a.tm_dv, dv, BH, N, d)) != FA_OK) return st;
+  if ((st = make_row_tile_map(&a.tm_q, q, BH, Nq, d, 64)) != FA_OK) return st;
+  if ((st = make_row_tile_map(&a.tm_k, k, BH, Nk, d, 128)) != FA_OK) return st;
+  if ((st = make_row_tile_map(&a.tm_v, v, BH, Nk, d, 128)) != FA_OK) return st;
+  if ((st = make_row_tile_map(&a.tm_do, dout, BH, Nq, d, 64)) != FA_OK) return st;
+  if ((st = make_grad_store_map(&a.tm_dk, dk, BH, Nk, d)) != FA_OK) return st;
+  if ((st = make_grad_store_map(&a.tm_dv, dv, BH, Nk, d)) != FA_OK) return st;
   a.o = o;
   a.dout = dout;
   a.lse = lse;
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
-  a.n_pad = static_cast<int>(round_up(static_cast<size_t>(N), 64));
+  a.n_pad = static_cast<int>(round_up(static_cast<size_t>(Nq), 64));
   a.bias = static_cast<uint8_t*>(workspace);
   a.B = B;
   a.H = H;
-  a.N = N;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.q_start = q_start;
   a.d = d;
   a.scale = resolve_scale(scale, d);
   a.scale_log2 = a.scale * kLog2e;
   a.causal = causal ? 1 : 0;
-  a.head_group = fa::head_group_for(a.causal, 2ll * N * d * 2 + static_cast<long long>(N) * d * 4, B * H);  // Q, dO, dQ
+  a.head_group = fa::head_group_for(a.causal, 2ll * Nq * d * 2 + static_cast<long long>(Nq) * d * 4, B * H);  // Q, dO, dQ
   a.o_f32 = (o_dtype == FA_F32) ? 1 : 0;
   a.stats = t_stats;
   const cudaError_t e = fa::launch_backward(a, static_cast<cudaStream_t>(stream));

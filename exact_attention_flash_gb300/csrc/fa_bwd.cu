@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
   // first to last across the group's heads (under causality key tile 0 meets the
   // most query tiles).  The longest blocks start first, which shortens the tail of
   // the grid, while only a group's Q, dO and dQ need to stay in L2.
-  const int n_kv = (a.N + kBKV - 1) / kBKV;
+  const int n_kv = (a.Nk + kBKV - 1) / kBKV;
   const int n_bh = a.B * a.H;
   const int hg = a.head_group;
   const int per_group = hg * n_kv;
@@ -143,9 +143,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
   const int bh = group * hg + g_idx % g_heads;
   const int j = g_idx / g_heads;
   const int key0 = j * kBKV;
-  const int n_q = (a.N + kBQ - 1) / kBQ;
-  const int i_start = a.causal ? key0 / kBQ : 0;
+  const int n_q = (a.Nq + kBQ - 1) / kBQ;
+  // Under causality query i (at position q_start + i) sees key j iff j <= q_start + i,
+  // so the first query block that sees any key of the tile holds query key0 - q_start.
+  const int i_start = a.causal ? static_cast<int>(max(0LL, static_cast<long long>(key0) - a.q_start) / kBQ) : 0;
   const int n_steps = n_q - i_start;
+  if (n_steps <= 0) {
+    // No query sees these keys (they lie after the last query's position): their
+    // gradients are zero.  Nothing else runs in this CTA.
+    const int rows = min(kBKV, a.Nk - key0);
+    float4* dk4 = reinterpret_cast<float4*>(a.dk + (static_cast<size_t>(bh) * a.Nk + key0) * D);
+    float4* dv4 = reinterpret_cast<float4*>(a.dv + (static_cast<size_t>(bh) * a.Nk + key0) * D);
+    for (int i = tid; i < rows * (D / 4); i += kBwdThreads) {
+      dk4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      dv4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
 
   if (tid == 0) {
     sh.abort = 0;
@@ -369,9 +383,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         break;
       }
       tc_fence_after();
-      const bool need_mask = (a.causal && key0 + kBKV - 1 > q0) || (key0 + kBKV > a.N);
-      const int first_visible_q = a.causal ? key : 0;  // queries before this key see nothing of it
-      const bool key_valid = key < a.N;
+      const bool need_mask = (a.causal && key0 + kBKV - 1 > a.q_start + q0) || (key0 + kBKV > a.Nk);
+      const int first_visible_q = a.causal ? key - a.q_start : 0;  // queries before this one see nothing of the key
+      const bool key_valid = key < a.Nk;
       const uint32_t s_tm = tmem_addr(tmem, lane_base, b * kBQ + 32 * h);
       const uint32_t dp_tm = tmem_addr(tmem, lane_base, 128 + b * kBQ + 32 * h);
       // P^T first, while the tensor core still computes dP^T.  S^T arrives holding
@@ -491,8 +505,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         // instruction then covers four whole 128-byte row segments, a quarter of the
         // instructions of one reduction per feature.
         const int i4 = lane & 3;
-        float* dst = a.dq + (static_cast<size_t>(bh) * a.N + q0 + i4) * D + lane_base + 4 * (lane >> 2);
-        const int rows = min(32, a.N - q0);
+        float* dst = a.dq + (static_cast<size_t>(bh) * a.Nq + q0 + i4) * D + lane_base + 4 * (lane >> 2);
+        const int rows = min(32, a.Nq - q0);
 #pragma unroll
         for (int kq = 0; kq < 8; ++kq) {
           const float x0 = __uint_as_float(v[4 * kq]) * a.scale, x1 = __uint_as_float(v[4 * kq + 1]) * a.scale;
@@ -611,7 +625,7 @@ cudaError_t launch_bwd_t(const BackwardArgs& a, cudaStream_t stream) {
   const long long padded_rows = static_cast<long long>(a.B) * a.H * a.n_pad;
   constexpr int kRowsPerBlock = 256 / (D / 8);
   bwd_preprocess<D><<<static_cast<unsigned>((padded_rows + kRowsPerBlock - 1) / kRowsPerBlock), 256, 0, stream>>>(
-      a.o, a.o_f32, static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.bias, a.dq, a.N, a.n_pad, padded_rows,
+      a.o, a.o_f32, static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.bias, a.dq, a.Nq, a.n_pad, padded_rows,
       1.f / a.scale);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -623,7 +637,7 @@ cudaError_t launch_bwd_t(const BackwardArgs& a, cudaStream_t stream) {
   e = cudaFuncGetAttributes(&attr, bwd_kernel<D>);
   if (e != cudaSuccess) return e;
   if (attr.numRegs * kBwdThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
-  const long long ctas = static_cast<long long>(a.B) * a.H * ((a.N + kBKV - 1) / kBKV);
+  const long long ctas = static_cast<long long>(a.B) * a.H * ((a.Nk + kBKV - 1) / kBKV);
   if (ctas > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   // A programmatic dependent of the preprocess kernel: its CTAs set up (barriers,
   // tensor memory, K and V) while the preprocess finishes, and wait for it only

@@ -100,7 +100,7 @@ struct FwdItem {
 // block has the most key tiles).  The longest items start first, which shortens the
 // tail, while only a group's K and V need to stay in L2.
 __device__ __forceinline__ FwdItem fwd_item(const ForwardArgs& a, int item) {
-  const int n_qblk = (a.N + kBM * kTiles - 1) / (kBM * kTiles);
+  const int n_qblk = (a.Nq + kBM * kTiles - 1) / (kBM * kTiles);
   const int n_bh = a.B * a.H;
   const int hg = a.head_group;
   const int per_group = hg * n_qblk;
@@ -110,10 +110,14 @@ __device__ __forceinline__ FwdItem fwd_item(const ForwardArgs& a, int item) {
   FwdItem w;
   w.bh = group * hg + g_idx % g_heads;
   w.q_row0 = (n_qblk - 1 - g_idx / g_heads) * (kBM * kTiles);
-  const int n_kv_total = (a.N + kBN - 1) / kBN;
+  const int n_kv_total = (a.Nk + kBN - 1) / kBN;
+  // Under causality the tile's last row, at position q_start + q_row0 + t kBM + kBM - 1,
+  // sees the keys up to that position.
 #pragma unroll
   for (int t = 0; t < kTiles; ++t)
-    w.n_kv[t] = a.causal ? min(n_kv_total, (w.q_row0 + t * kBM) / kBN + 1) : n_kv_total;
+    w.n_kv[t] = a.causal ? static_cast<int>(min(static_cast<long long>(n_kv_total),
+                                                (static_cast<long long>(a.q_start) + w.q_row0 + t * kBM + kBM - 1) / kBN + 1))
+                         : n_kv_total;
   return w;
 }
 
@@ -134,7 +138,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   // the MMA issuer and the softmax warps through a two-slot ring.  The barriers'
   // phases run on across items (one K/V ring, per-tile step counters, one Q and O
   // hand-off per item).
-  const int n_items = a.B * a.H * ((a.N + kBM * kTiles - 1) / (kBM * kTiles));
+  const int n_items = a.B * a.H * ((a.Nq + kBM * kTiles - 1) / (kBM * kTiles));
 
   if (tid == 0) {
     bars.abort = 0;
@@ -282,7 +286,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         // fa_set_stats counters: S products of query tiles that start before N, and
         // the key tiles causality skipped for them.
         unsigned n_tiles = 0, n_skipped = 0;
-        const int n_kv_total = (a.N + kBN - 1) / kBN;
+        const int n_kv_total = (a.Nk + kBN - 1) / kBN;
         bool ok = true;
         for (int it = 0; ok; ++it) {
           const int r = it % kItemRing;
@@ -293,7 +297,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           const FwdItem w = fwd_item(a, item);
 #pragma unroll
           for (int t = 0; t < kTiles; ++t)
-            if (w.q_row0 + t * kBM < a.N) {
+            if (w.q_row0 + t * kBM < a.Nq) {
               n_tiles += w.n_kv[t];
               n_skipped += n_kv_total - w.n_kv[t];
             }
@@ -396,9 +400,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         for (int i = 0; i < 64; ++i) x[64 + i] = __uint_as_float(u[i]);
       }
       const int key0 = j * kBN;
-      const bool need_mask = (key0 + kBN > a.N) || (a.causal && key0 + kBN - 1 > q_row0 + t * kBM);
+      const bool need_mask = (key0 + kBN > a.Nk) || (a.causal && key0 + kBN - 1 > a.q_start + q_row0 + t * kBM);
       if (need_mask) {
-        const int lim = a.causal ? min(a.N - 1, row) : a.N - 1;  // last visible key
+        const int lim = a.causal ? min(a.Nk - 1, a.q_start + row) : a.Nk - 1;  // last visible key
 #pragma unroll
         for (int i = 0; i < kBN; ++i)
           if (key0 + i > lim) x[i] = -INFINITY;
@@ -413,7 +417,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         mx8[c] = fmaxf(v, x[16 * c + 15]);
       }
       const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-      n_rescales += (row < a.N && mx > mx_seen && mx_seen != -INFINITY) ? 1u : 0u;
+      n_rescales += (row < a.Nq && mx > mx_seen && mx_seen != -INFINITY) ? 1u : 0u;
       mx_seen = fmaxf(mx_seen, mx);
       const float m_tile = mx * sl2;
       float m_use = m_run;
@@ -509,11 +513,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     mbar_arrive(&bars.o_empty[t]);
     {
       const float inv_l = 1.f / l_hat;
-      const size_t row_off = (static_cast<size_t>(bh) * a.N + row) * D;
+      const size_t row_off = (static_cast<size_t>(bh) * a.Nq + row) * D;
 #pragma unroll
       for (int c = 0; c < D; c += 32) {
         const uint32_t* u = orow + c;
-        if (row < a.N) {
+        if (row < a.Nq) {
           if (a.o_f32) {
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.o) + row_off + c);
 #pragma unroll
@@ -533,7 +537,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           }
         }
       }
-      if (row < a.N) a.lse[static_cast<size_t>(bh) * a.N + row] = (m_run + __log2f(l_run)) * kLn2;
+      if (row < a.Nq) a.lse[static_cast<size_t>(bh) * a.Nq + row] = (m_run + __log2f(l_run)) * kLn2;
     }
     }
     if (a.stats != nullptr) {  // fa_set_stats counters: one addition per warp and CTA
@@ -570,7 +574,7 @@ cudaError_t launch_fwd_t(const ForwardArgs& a, cudaStream_t stream) {
   e = cudaFuncGetAttributes(&attr, fwd_kernel<D, kPrecise>);
   if (e != cudaSuccess) return e;
   if (attr.numRegs * kFwdThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
-  const long long items = static_cast<long long>(a.B) * a.H * ((a.N + kBM * kTiles - 1) / (kBM * kTiles));
+  const long long items = static_cast<long long>(a.B) * a.H * ((a.Nq + kBM * kTiles - 1) / (kBM * kTiles));
   if (items > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   // Persistent grid: one CTA per SM (each needs a whole SM's tensor memory), each
   // walking its share of the items.

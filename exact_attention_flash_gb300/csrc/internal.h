@@ -9,10 +9,11 @@
 namespace fa {
 
 struct ForwardArgs {
-  CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps over [B*H, N, d] bf16, box {64, 128, 1}, 128B swizzle
-  void* o;                       // [B, H, N, d] bf16 or fp32
-  float* lse;                    // [B, H, N] natural-log log-sum-exp
-  int B, H, N, d;
+  CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps over [B*H, Nq or Nk, d] bf16, box {64, 128, 1}, 128B swizzle
+  void* o;                       // [B, H, Nq, d] bf16 or fp32
+  float* lse;                    // [B, H, Nq] natural-log log-sum-exp
+  int B, H, Nq, Nk, d;
+  int q_start;                   // absolute position of query row 0 (causal: key j visible iff j <= q_start + i)
   float scale_log2;              // scale * log2(e)
   int causal;
   int o_f32;                     // 1: O is fp32, 0: bf16
@@ -23,18 +24,19 @@ struct ForwardArgs {
 };
 
 struct BackwardArgs {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 3-D maps over [B*H, N, d] bf16; Q, dO boxes of 64 rows, K, V of 128
-  CUtensorMap tm_dk, tm_dv;             // 3-D maps over dK, dV [B*H, N, d] fp32, box {32, 128, 1}, 128B swizzle
-  const void* o;                        // [B, H, N, d] bf16 or fp32
-  const void* dout;                     // [B, H, N, d] bf16
-  const float* lse;                     // [B, H, N]
-  float* dq;                            // [B, H, N, d] fp32 (accumulated into; zeroed by the launcher)
-  float* dk;                            // [B, H, N, d] fp32
-  float* dv;                            // [B, H, N, d] fp32
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 3-D maps over [B*H, Nq or Nk, d] bf16; Q, dO boxes of 64 rows, K, V of 128
+  CUtensorMap tm_dk, tm_dv;             // 3-D maps over dK, dV [B*H, Nk, d] fp32, box {32, 128, 1}, 128B swizzle
+  const void* o;                        // [B, H, Nq, d] bf16 or fp32
+  const void* dout;                     // [B, H, Nq, d] bf16
+  const float* lse;                     // [B, H, Nq]
+  float* dq;                            // [B, H, Nq, d] fp32 (accumulated into; zeroed by the launcher)
+  float* dk;                            // [B, H, Nk, d] fp32
+  float* dv;                            // [B, H, Nk, d] fp32
   uint8_t* bias;                        // workspace [B*H, n_pad / 64] blocks of 4 KB: per 64-query block the
-                                        // bias tiles -LSE/scale and -rowsum(dO * O) (-inf and 0 past N)
-  int n_pad;                            // N rounded up to a multiple of 64
-  int B, H, N, d;
+                                        // bias tiles -LSE/scale and -rowsum(dO * O) (-inf and 0 past Nq)
+  int n_pad;                            // Nq rounded up to a multiple of 64
+  int B, H, Nq, Nk, d;
+  int q_start;                          // absolute position of query row 0, as in the forward
   float scale;                          // softmax scale
   float scale_log2;                     // scale * log2(e)
   int causal;

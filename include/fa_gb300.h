@@ -72,7 +72,26 @@ const char* fa_status_string(fa_status s);
 fa_status fa_forward(const void* q, const void* k, const void* v, void* o, fa_dtype o_dtype, float* lse, int B,
                      int H, int N, int d, float scale, int causal, int precise, void* stream);
 
-/* Bytes of workspace fa_backward needs: 64 per query row over N rounded up to a
+/*
+ * fa_forward_qk — fa_forward with Nq queries against Nk keys and a query offset.
+ *
+ * Defines: "attention_kernels.py" section 3 ``flash_forward`` with its ``q_start``
+ * (section 2 ``_mask``): query row i sits at absolute position q_start + i and,
+ * with causal != 0, sees key j iff j <= q_start + i.  Without causal every query
+ * sees every key (cross-attention when Nq != Nk).  Covers chunked prefill
+ * (q_start = Nk - Nq) and multi-token decoding with a causal mask.
+ *
+ *  q   [B, H, Nq, d] bf16;  k, v  [B, H, Nk, d] bf16.
+ *  o   [B, H, Nq, d] in o_dtype, written;  lse  [B, H, Nq] float, written.
+ *  Nq, Nk >= 1;  q_start >= 0 (every query then sees key 0) and q_start + Nq
+ *  must fit in int: otherwise FA_ERR_INVALID_ARG.  fa_forward(..., N, ...) is
+ *  fa_forward_qk(..., Nq = Nk = N, q_start = 0, ...).
+ */
+fa_status fa_forward_qk(const void* q, const void* k, const void* v, void* o, fa_dtype o_dtype, float* lse, int B,
+                        int H, int Nq, int Nk, int q_start, int d, float scale, int causal, int precise,
+                        void* stream);
+
+/* Bytes of workspace fa_backward needs (pass Nq for fa_backward_qk): 64 per query row over N rounded up to a
  * multiple of 64 (per row, -LSE/scale and -rowsum(dO * O), each as three bf16
  * terms, laid out as tensor-core operand tiles). */
 size_t fa_backward_workspace_size(int B, int H, int N, int d);
@@ -94,6 +113,25 @@ size_t fa_backward_workspace_size(int B, int H, int N, int d);
 fa_status fa_backward(const void* q, const void* k, const void* v, const void* o, fa_dtype o_dtype,
                       const float* lse, const void* dout, float* dq, float* dk, float* dv, int B, int H, int N, int d,
                       float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fa_backward_qk — fa_backward with Nq queries against Nk keys and a query offset.
+ *
+ * Defines: the gradient of fa_forward_qk's result ("attention_kernels.py"
+ * section 4 ``flash_backward``, whose recompute of P uses the same mask as the
+ * forward).  Keys no query sees (positions after q_start + Nq - 1 under causal)
+ * get zero dK and dV.
+ *
+ *  q, dout, o  [B, H, Nq, d];  lse [B, H, Nq];  k, v [B, H, Nk, d].
+ *  dq [B, H, Nq, d] float;  dk, dv [B, H, Nk, d] float, written.
+ *  workspace   >= fa_backward_workspace_size(B, H, Nq, d) bytes.
+ * Lengths and offset as for fa_forward_qk; they, causal and scale must match
+ * the forward call.
+ */
+fa_status fa_backward_qk(const void* q, const void* k, const void* v, const void* o, fa_dtype o_dtype,
+                         const float* lse, const void* dout, float* dq, float* dk, float* dv, int B, int H, int Nq,
+                         int Nk, int q_start, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
+                         void* stream);
 
 /* Bytes of workspace fa_decode needs: per-segment states and one arrival
  * counter per (batch, head). */

@@ -82,6 +82,19 @@ def test_decode_rejects_bad_arguments(lib):
     assert lib.fa_debug_wait_timeout(0, None) == 1
 
 
+def test_offset_entry_points_reject_bad_arguments(lib):
+    # fa_forward_qk(q, k, v, o, o_dtype, lse, B, H, Nq, Nk, q_start, d, scale, causal, precise, stream)
+    assert lib.fa_forward_qk(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 16, -1, 64, 0.0, 1, 0, None) == 1
+    assert lib.fa_forward_qk(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 0, 0, 64, 0.0, 1, 0, None) == 1
+    assert lib.fa_forward_qk(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 16, 2**31 - 4, 64, 0.0, 1, 0, None) == 1
+    assert lib.fa_forward_qk(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 16, 0, 48, 0.0, 1, 0, None) == 2
+    args = [FAKE] * 4 + [0, FAKE, FAKE, FAKE, FAKE, FAKE]
+    # fa_backward_qk(..., B, H, Nq, Nk, q_start, d, scale, causal, workspace, bytes, stream)
+    assert lib.fa_backward_qk(*args, 1, 1, 8, 16, -3, 64, 0.0, 1, FAKE, 1 << 20, None) == 1
+    assert lib.fa_backward_qk(*args, 1, 1, 8, 0, 0, 64, 0.0, 1, FAKE, 1 << 20, None) == 1
+    assert lib.fa_backward_qk(*args, 1, 1, 8, 16, 0, 64, 0.0, 1, FAKE, 4, None) == 5
+
+
 def test_set_stats_arguments(lib):
     # the counters must be 8-byte aligned; NULL stops counting (nothing runs here)
     assert lib.fa_set_stats(FAKE + 4) == 1
