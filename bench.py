@@ -487,9 +487,8 @@ def run_all_workloads(reps):
     """One JSON line per named workload and kernel family: each call timed alone
     with CUDA events (median of `reps`), with L2 flushed by a 256 MB write before
     every timed call, so that small workloads are not timed from a warm L2."""
-    import statistics
-
-    from exact_attention_flash_gb300 import backward_workspace_bytes, fa_backward, fa_decode, fa_forward
+    from exact_attention_flash_gb300 import (backward_workspace_bytes, decode_auto_split, fa_backward, fa_decode,
+                                             fa_forward, fa_merge_states)
     from exact_attention_flash_gb300.build import build
     from exact_attention_flash_gb300.workloads import WORKLOADS, make_attention_inputs, make_decode_inputs
 
@@ -497,7 +496,31 @@ def run_all_workloads(reps):
     peaks = load_peaks()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for name, w in WORKLOADS.items():
+    # Beyond the named workloads: the merge of two fp32 results of the bench forward's
+    # shape, and the decode workload with the library's automatic split count.
+    extra = {}
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    m_shape = (2, 16, 8192)
+    m_in = [torch.randn(m_shape + (128,), generator=g, device="cuda") for _ in range(2)]
+    m_lse = [torch.randn(m_shape, generator=g, device="cuda") for _ in range(2)]
+    m_out, m_out_lse = torch.empty_like(m_in[0]), torch.empty_like(m_lse[0])
+    rows = m_lse[0].numel()
+    extra["merge_b2h16_n8192_d128_f32"] = {"merge": (
+        lambda: fa_merge_states(m_in[0], m_lse[0], m_in[1], m_lse[1], out=m_out, lse=m_out_lse),  # noqa: E731
+        3 * rows * 128 * 4 + 3 * rows * 4, "GB/s")}
+    wd = WORKLOADS["decode_b16h32_l32768_d128_s64"]
+    qa, ka, va = make_decode_inputs(wd.B, wd.H, wd.N, wd.d, wd.seed, "cuda")
+    n_auto = decode_auto_split(wd.B, wd.H, wd.N)
+    oa, la = fa_decode(qa, ka, va, n_auto)
+    extra[f"decode_b16h32_l32768_d128_auto{n_auto}"] = {"decode": (
+        lambda: fa_decode(qa, ka, va, n_auto, out=oa, lse=la),  # noqa: E731
+        decode_bytes(wd.B, wd.H, wd.N, wd.d, n_auto), "GB/s")}
+    for name, w in list(WORKLOADS.items()) + list(extra.items()):
+        if isinstance(w, dict):
+            calls = w
+            _time_calls(name, calls, reps, flush, e0, e1, peaks)
+            continue
         calls = {}
         if w.kind == "decode":
             q, k, v = make_decode_inputs(w.B, w.H, w.N, w.d, w.seed, "cuda")
@@ -515,24 +538,30 @@ def run_all_workloads(reps):
                 ws = torch.empty(backward_workspace_bytes(w.B, w.H, w.N, w.d), device="cuda", dtype=torch.uint8)
                 calls["backward"] = (lambda: fa_backward(q, k, v, o, lse, do, causal=w.causal, workspace=ws),  # noqa: E731
                                      attention_flops(w.B, w.H, w.N, w.d, w.causal, True), "TFLOP/s")
-        for kname, (fn, work, unit) in calls.items():
-            for _ in range(3):
-                fn()
-            times = []
-            for _ in range(reps):
-                flush.zero_()
-                e0.record()
-                fn()
-                e1.record()
-                torch.cuda.synchronize()
-                times.append(e0.elapsed_time(e1))
-            ms = statistics.median(times)
-            rate = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
-            peak = peaks["bf16_tflops"] if unit == "TFLOP/s" else peaks["hbm_gbs"]
-            print(json.dumps({"workload": name, "kernel": kname, "ms": ms, "rate": rate, "unit": unit,
-                              "frac_of_measured_peak": rate / peak, "reps": reps, "l2": "flushed before each call"}))
+        _time_calls(name, calls, reps, flush, e0, e1, peaks)
         del calls
         torch.cuda.empty_cache()
+
+
+def _time_calls(name, calls, reps, flush, e0, e1, peaks):
+    """Time each (fn, work, unit) of `calls` alone: median of `reps` CUDA-event timings,
+    L2 flushed before each; print one JSON line per kernel."""
+    for kname, (fn, work, unit) in calls.items():
+        for _ in range(3):
+            fn()
+        times = []
+        for _ in range(reps):
+            flush.zero_()
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        rate = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
+        peak = peaks["bf16_tflops"] if unit == "TFLOP/s" else peaks["hbm_gbs"]
+        print(json.dumps({"workload": name, "kernel": kname, "ms": ms, "rate": rate, "unit": unit,
+                          "frac_of_measured_peak": rate / peak, "reps": reps, "l2": "flushed before each call"}))
 
 
 def main():

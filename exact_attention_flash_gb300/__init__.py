@@ -6,15 +6,16 @@ kernels of ``libfa_gb300.so`` reached through its C ABI (``include/fa_gb300.h``)
 """
 from __future__ import annotations
 
+import contextlib
+
 import torch
 
 from . import _lib
 from ._lib import FAError
 
 __all__ = ["fa_forward", "fa_backward", "fa_decode", "fa_device_status", "FAError", "backward_workspace_bytes",
-           "decode_workspace_bytes", "fa_set_stats", "stats_counters", "STATS_FIELDS"]
-
-import contextlib
+           "decode_workspace_bytes", "fa_set_stats", "stats_counters", "STATS_FIELDS", "fa_merge_states",
+           "decode_auto_split"]
 
 # Order of the counters behind fa_set_stats ("attention_kernels.py" sections 3-4, ``stats``).
 STATS_FIELDS = ("tiles", "skipped", "rescales", "dq_atomic_adds")
@@ -116,9 +117,20 @@ def decode_workspace_bytes(B, H, d, n_split) -> int:
     return int(_lib.load().fa_decode_workspace_size(B, H, d, n_split))
 
 
-def fa_decode(q, k, v, n_split, scale=None, return_partials=False, workspace=None, out=None, lse=None,
+def decode_auto_split(B, H, L) -> int:
+    """The library's split count for B * H heads of L keys on the current device."""
+    n = int(_lib.load().fa_decode_auto_split(B, H, L))
+    if n < 1:
+        raise ValueError("fa_decode_auto_split: bad sizes or no device")
+    return n
+
+
+def fa_decode(q, k, v, n_split=None, scale=None, return_partials=False, workspace=None, out=None, lse=None,
               stream=None):
-    """Split-KV decode: q [B, H, 1, d], k/v [B, H, L, d] bf16 -> O [B, H, 1, d] fp32, LSE [B, H]."""
+    """Split-KV decode: q [B, H, 1, d], k/v [B, H, L, d] bf16 -> O [B, H, 1, d] fp32, LSE [B, H].
+
+    ``n_split=None`` takes :func:`decode_auto_split`'s count.
+    """
     lib = _lib.load()
     _check_bf16("q", q)
     _check_bf16("k", k)
@@ -126,11 +138,15 @@ def fa_decode(q, k, v, n_split, scale=None, return_partials=False, workspace=Non
     B, H, L, d = k.shape
     if tuple(q.shape) != (B, H, 1, d):
         raise ValueError("q must be [B, H, 1, d]")
+    if n_split is None:
+        n_split = decode_auto_split(B, H, L)
     if workspace is None:
         workspace = torch.empty(decode_workspace_bytes(B, H, d, max(int(n_split), 1)), device=q.device,
                                 dtype=torch.uint8)
     out = torch.empty((B, H, 1, d), device=q.device, dtype=torch.float32) if out is None else out
     lse = torch.empty((B, H), device=q.device, dtype=torch.float32) if lse is None else lse
+    _check_out("out", out, (B, H, 1, d), (torch.float32,))
+    _check_out("lse", lse, (B, H), (torch.float32,))
     parts = None
     if return_partials:
         parts = torch.empty((B, H, max(int(n_split), 1), d + 2), device=q.device, dtype=torch.float32)
@@ -171,3 +187,30 @@ def stats_counters(device=None):
         yield c
     finally:
         fa_set_stats(None)
+
+
+def fa_merge_states(o_a, lse_a, o_b, lse_b, out=None, lse=None, stream=None):
+    """Merge two attention results over disjoint key sets ("attention_kernels.py" section 1 ``merge_states``).
+
+    o_a, o_b: [..., d] fp32 or bf16 (one shape and dtype); lse_a, lse_b: [...] fp32.
+    Returns (O, LSE) of the attention over both key sets; ``out`` and ``lse`` may
+    be the inputs (in place).
+    """
+    lib = _lib.load()
+    if o_a.dtype != o_b.dtype or o_a.dtype not in (torch.float32, torch.bfloat16) or o_a.shape != o_b.shape:
+        raise ValueError("o_a and o_b must have one shape and dtype (fp32 or bf16)")
+    d = o_a.shape[-1]
+    lead = tuple(o_a.shape[:-1])
+    for name, t in (("o_a", o_a), ("o_b", o_b)):
+        _check_out(name, t, o_a.shape, (o_a.dtype,))
+    for name, t in (("lse_a", lse_a), ("lse_b", lse_b)):
+        _check_out(name, t, lead, (torch.float32,))
+    out = torch.empty_like(o_a) if out is None else out
+    lse = torch.empty_like(lse_a) if lse is None else lse
+    _check_out("out", out, o_a.shape, (o_a.dtype,))
+    _check_out("lse", lse, lead, (torch.float32,))
+    code = lib.fa_merge_states(o_a.data_ptr(), lse_a.data_ptr(), o_b.data_ptr(), lse_b.data_ptr(), out.data_ptr(),
+                               lse.data_ptr(), _lib.FA_F32 if o_a.dtype == torch.float32 else _lib.FA_BF16,
+                               lse_a.numel(), d, _stream_ptr(stream))
+    _lib.check("fa_merge_states", code)
+    return out, lse

@@ -252,6 +252,32 @@ fa_status fa_device_status(void* stream) {
   return FA_OK;
 }
 
+fa_status fa_merge_states(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o,
+                          float* lse, fa_dtype o_dtype, long long rows, int d, void* stream) {
+  if (!o_a || !lse_a || !o_b || !lse_b || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(o_a) || !aligned16(o_b) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  const uintptr_t l4 = reinterpret_cast<uintptr_t>(lse_a) | reinterpret_cast<uintptr_t>(lse_b) |
+                       reinterpret_cast<uintptr_t>(lse);
+  if ((l4 & 3u) != 0) return FA_ERR_INVALID_ARG;
+  if (o_dtype != FA_BF16 && o_dtype != FA_F32) return FA_ERR_INVALID_ARG;
+  if (rows < 0 || d < 4 || d % 4 != 0 || d > 4096) return FA_ERR_INVALID_ARG;
+  if (rows == 0) return FA_OK;
+  return fa::launch_merge(o_a, lse_a, o_b, lse_b, o, lse, rows, d, o_dtype == FA_F32 ? 1 : 0,
+                          static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
+int fa_decode_auto_split(int B, int H, int L) {
+  if (B < 1 || H < 1 || L < 1) return 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms < 1)
+    return 0;
+  const long long bh = static_cast<long long>(B) * H;
+  return fa::decode_auto_split(bh > 0x7FFFFFFFLL ? 0x7FFFFFFF : static_cast<int>(bh), L, sms);
+}
+
 fa_status fa_set_stats(unsigned long long* counters) {
   if ((reinterpret_cast<uintptr_t>(counters) & 7u) != 0) return FA_ERR_INVALID_ARG;
   t_stats = counters;

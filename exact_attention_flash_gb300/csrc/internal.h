@@ -78,6 +78,14 @@ cudaError_t launch_forward(const ForwardArgs& a, cudaStream_t stream);
 cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
+// Merge of two (O, LSE) results over disjoint key sets (fa_merge.cu); o_f32: O is
+// fp32, else bf16.  O rows of d elements, d a multiple of 4.
+cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o, float* lse,
+                         long long rows, int d, int o_f32, cudaStream_t stream);
+
+// Split count of the decode path for B*H heads of L keys on `sms` SMs.
+int decode_auto_split(int BH, int L, int sms);
+
 // Device status words, one per kernel file: read and cleared on `stream`.
 cudaError_t read_clear_forward_status(unsigned* out, cudaStream_t stream);
 cudaError_t read_clear_backward_status(unsigned* out, cudaStream_t stream);

@@ -159,6 +159,19 @@ fa_status fa_decode(const void* q, const void* k, const void* v, float* o, float
                     float scale, int n_split, float* partials, void* workspace, size_t workspace_bytes,
                     void* stream);
 
+/*
+ * fa_decode_auto_split — a split count for fa_decode: B * H heads of L keys on
+ * the current device.  Returns n_split >= 1, or 0 if an argument is < 1 or the
+ * device cannot be queried.
+ *
+ * The pages leave n_split to the caller ("attention_kernels.py" section 5).  The
+ * rule, from measurements of fa_decode on GB300 over n_split in 1..256: about
+ * four CTAs per SM in all (ceil(4 * SMs / (B * H)) splits), at least 8, and no
+ * segment shorter than 512 keys (at most L / 512 splits, at least 1).  Size the
+ * workspace with the same n_split.
+ */
+int fa_decode_auto_split(int B, int H, int L);
+
 /* Size in bytes of the fixed scratch array behind fa_decode_noalloc. */
 #define FA_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20)
 
@@ -196,6 +209,29 @@ fa_status fa_decode_noalloc(const void* q, const void* k, const void* v, float* 
  * wait since the last call, FA_ERR_CUDA if the CUDA calls fail, else FA_OK.
  */
 fa_status fa_device_status(void* stream);
+
+/*
+ * fa_merge_states — combines two attention results over disjoint key sets.
+ *
+ * Defines: "attention_kernels.py" section 1 ``merge_states``: softmax states
+ * (m, l, o) of two runs of scores merge as m = max(m_a, m_b),
+ * l = l_a e^(m_a - m) + l_b e^(m_b - m), o likewise.  A normalised result
+ * (O, LSE) is the state (LSE, 1, O), so per row, with m = max(LSE_a, LSE_b) and
+ * w = e^(LSE - m):  LSE = m + ln(w_a + w_b),  O = (w_a O_a + w_b O_b) / (w_a + w_b).
+ * LSE = -inf marks an empty run, the identity; two empty runs give O = 0 and
+ * LSE = -inf.  Typical use: attention over keys held in two pieces (two
+ * fa_forward_qk calls without causality, or two fa_decode calls), merged into
+ * the result over all keys.
+ *
+ *  o_a, o_b, o      rows x d, contiguous per row, in o_dtype (FA_F32 or
+ *                   FA_BF16); 16-byte aligned.  o may be o_a or o_b.
+ *  lse_a, lse_b, lse  rows floats (natural log); lse may be lse_a or lse_b.
+ *  rows >= 0 (0 queues nothing);  d a multiple of 4 in [4, 4096].
+ * Returns FA_OK when queued; FA_ERR_INVALID_ARG for null or misaligned
+ * pointers or bad sizes.
+ */
+fa_status fa_merge_states(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o,
+                          float* lse, fa_dtype o_dtype, long long rows, int d, void* stream);
 
 /*
  * fa_set_stats — counters of the pages' ``stats`` dictionary, for debugging and

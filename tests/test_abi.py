@@ -95,6 +95,19 @@ def test_offset_entry_points_reject_bad_arguments(lib):
     assert lib.fa_backward_qk(*args, 1, 1, 8, 16, 0, 64, 0.0, 1, FAKE, 4, None) == 5
 
 
+def test_merge_and_auto_split_reject_bad_arguments(lib):
+    # fa_merge_states(o_a, lse_a, o_b, lse_b, o, lse, o_dtype, rows, d, stream)
+    assert lib.fa_merge_states(None, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 128, None) == 1
+    assert lib.fa_merge_states(FAKE + 8, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 128, None) == 1
+    assert lib.fa_merge_states(FAKE, FAKE + 2, FAKE, FAKE, FAKE, FAKE, 1, 4, 128, None) == 1
+    assert lib.fa_merge_states(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 126, None) == 1
+    assert lib.fa_merge_states(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 3, 4, 128, None) == 1
+    assert lib.fa_merge_states(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, -1, 128, None) == 1
+    assert lib.fa_merge_states(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 0, 128, None) == 0  # nothing to do
+    assert lib.fa_decode_auto_split(0, 1, 100) == 0
+    assert lib.fa_decode_auto_split(1, 1, 0) == 0
+
+
 def test_set_stats_arguments(lib):
     # the counters must be 8-byte aligned; NULL stops counting (nothing runs here)
     assert lib.fa_set_stats(FAKE + 4) == 1
