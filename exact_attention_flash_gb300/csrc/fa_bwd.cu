@@ -171,10 +171,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.s_full[b], 1);
       mbar_init(&sh.dp_full[b], 1);
-      mbar_init(&sh.p_full[b], 256);
-      mbar_init(&sh.ds_full[b], 256);
+      mbar_init(&sh.p_full[b], 8);   // one arrival per P/dS warp
+      mbar_init(&sh.ds_full[b], 8);
       mbar_init(&sh.dq_full[b], 1);
-      mbar_init(&sh.dq_empty[b], 256);
+      mbar_init(&sh.dq_empty[b], 8); // one arrival per dQ writer warp
       mbar_init(&sh.ds_empty[b], 1);
     }
     mbar_init(&sh.dkdv_full, 1);
@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       // columns, which this thread has already read.
       tmem_st16(s_tm, pk);
       tc_fence_before();
-      mbar_arrive(&sh.p_full[b]);
+      mbar_arrive_warp(&sh.p_full[b]);
       if (!__all_sync(0xffffffffu, mbar_wait(&sh.dp_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status))) {
         ok = false;
         break;
@@ -437,7 +437,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       tmem_st16(dp_tm, dk);
       tc_fence_before();
       fence_proxy_async_smem();
-      mbar_arrive(&sh.ds_full[b]);
+      mbar_arrive_warp(&sh.ds_full[b]);
     }
     // ------------------------------------------------------------ dK, dV epilogue
     // Once the last products are done, the Q/dO/dS buffers are free: dK and dV are
@@ -497,7 +497,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       tc_fence_after();
       if (has_rows) tmem_ld32(tmem_addr(tmem, lane_base, 128 + b * kBQ + 32 * half), v);
       tc_fence_before();
-      mbar_arrive(&sh.dq_empty[b]);
+      mbar_arrive_warp(&sh.dq_empty[b]);
       if (has_rows) {
         // 4 x 4 transposes within each group of four lanes (two shuffle rounds per
         // block of four queries): lane 4g + i ends up with features 4g .. 4g + 3 of

@@ -75,7 +75,7 @@ struct FwdCfg {
 };
 
 constexpr int kItemRing = 2;
-constexpr int kItemReaders = 32 + 2 * kBM;  // the MMA warp and the softmax warps
+constexpr int kItemReaders = 1 + 2 * kBM / 32;  // arrivals per warp: the MMA warp and the softmax warps
 
 struct FwdBarriers {
   uint64_t item_full[kItemRing], item_empty[kItemRing];
@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(&bars.q_full[t], 1);
       mbar_init(&bars.q_empty[t], 1);
-      mbar_init(&bars.o_empty[t], kBM);
+      mbar_init(&bars.o_empty[t], kBM / 32);  // one arrival per softmax warp of the tile
     }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars.k_full[s], 1);
@@ -158,8 +158,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     }
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(&bars.s_full[t], 1);
-      mbar_init(&bars.p_half[t], kBM);
-      mbar_init(&bars.p_full[t], kBM);
+      mbar_init(&bars.p_half[t], kBM / 32);  // one arrival per softmax warp of the tile
+      mbar_init(&bars.p_full[t], kBM / 32);
       mbar_init(&bars.o_full[t], 1);
     }
     mbar_init(&bars.drain, 1);
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           const int r = it % kItemRing;
           if (!warp_wait(&bars.item_full[r], (it / kItemRing) & 1, &bars.abort, &g_fwd_status)) break;
           const int item = bars.item[r];
-          mbar_arrive(&bars.item_empty[r]);
+          mbar_arrive_warp(&bars.item_empty[r]);
           if (item >= n_items) break;
           const FwdItem w = fwd_item(a, item);
 #pragma unroll
@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     if (!__all_sync(0xffffffffu, mbar_wait(&bars.item_full[ring], (it / kItemRing) & 1, &bars.abort, &g_fwd_status)))
       break;
     const int item = bars.item[ring];
-    mbar_arrive(&bars.item_empty[ring]);
+    mbar_arrive_warp(&bars.item_empty[ring]);
     if (item >= n_items) break;
     const FwdItem w = fwd_item(a, item);
     const int q_row0 = w.q_row0, bh = w.bh;
@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         tmem_st32(s_tm + half * 32, u);
         if (!kPrecise && half == 0) {  // keys 0..63 are ready for the PV product
           tc_fence_before();
-          mbar_arrive(&bars.p_half[t]);
+          mbar_arrive_warp(&bars.p_half[t]);
         }
       }
       if (kPrecise) {  // residuals over columns 64..127 (the S values there are consumed)
@@ -492,8 +492,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       l_hat = kPrecise ? l_run : l_hat * alpha + (rowsum + delta_max);
       m_run = m_use;
       tc_fence_before();
-      if (kPrecise) mbar_arrive(&bars.p_half[t]);
-      mbar_arrive(&bars.p_full[t]);
+      if (kPrecise) mbar_arrive_warp(&bars.p_half[t]);
+      mbar_arrive_warp(&bars.p_full[t]);
     }
     // ------------------------------------------------------------ epilogue
     // The whole O row leaves tensor memory first; o_empty then lets the next item's
@@ -510,7 +510,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       tmem_ld64(o_tm + c, part);
     }
     tc_fence_before();
-    mbar_arrive(&bars.o_empty[t]);
+    mbar_arrive_warp(&bars.o_empty[t]);
     {
       const float inv_l = 1.f / l_hat;
       const size_t row_off = (static_cast<size_t>(bh) * a.Nq + row) * D;

@@ -86,6 +86,14 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 
 constexpr uint32_t kWaitSleepNs = 20000;  // per sleeping try; the deadline is checked between tries
 
+// One arrival for a whole warp: __syncwarp orders every lane's earlier writes before
+// lane 0's release-arrival, so a barrier that counts warps instead of threads sees
+// the same writes with 1/32 of the shared-memory atomics.
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31u) == 0) mbar_arrive(bar);
+}
+
 // Wait until the barrier's phase with the given parity has completed.
 // Returns false (and raises *abort, sets kDevTimeout in *status) on timeout,
 // or false at once if another role of the CTA has already raised *abort.
