@@ -24,7 +24,8 @@ Sources (web pages on exact tiled attention; cited by title and section):
   gradient).
 * "flash_attention_numpy.py" (first_principles, flash-attention tier 1):
   ``standard_attention`` with *unscaled* scores (scale = 1), used by the
-  worked N=3, d=2 example.
+  worked N=3, d=2 example, and ``flash_attention_tier1`` (the first
+  algorithm's key-major loop order).
 
 Pins (what each function is checked against, in ``tests/test_oracle_*.py``):
 the printed N=3, d=2 example and hand-derived closed forms of it, uniform
@@ -337,6 +338,56 @@ def attention_flash_blocked_backward(q, k, v, out, lse, do, br, bc, scale=None, 
             dk[j0:j1] += (ds.T @ q[i0:i1]) * sc
             _bump(stats, "dq_atomic_adds", (i1 - i0) * q.shape[1])
     return dq, dk, dv
+
+
+def attention_fa1_keymajor(q, k, v, br, bc, scale=None, causal=False):
+    """The first algorithm's loop order: key blocks outer, query blocks inner.
+
+    The running output O, maximum m and sum r of every query row live outside the
+    loops and are repaired at each visit: for key block j and query block i, with
+    the block's scores s, m~ = rowmax s, p~ = exp(s - m~), r~ = rowsum p~;
+    m' = max(m, m~), r' = e^(m - m') r + e^(m~ - m') r~, and
+    O = (e^(m - m') r / r') O + e^(m~ - m') (p~ V_j) / r'; then m, r = m', r'.  O is
+    normalised after every visit.  Rows whose scores in a block are all masked take
+    nothing from it (their m~ is -inf).  Returns O and L = m + log r.
+    Source: "flash_attention_numpy.py" ``flash_attention_tier1`` (unscaled, no
+    mask); the scale and the causal skip and mask follow "attention_kernels.py"
+    section 3.  Single head: q (N, d), k (N, d), v (N, dv).
+    """
+    if br < 1 or bc < 1:
+        raise ValueError("block sizes must be >= 1")
+    q, k, v = _as_f64(q, k, v)
+    sc = default_scale(q.shape[1], scale)
+    n = q.shape[0]
+    out = np.zeros((n, v.shape[1]))
+    m = np.full(n, NEG_INF)
+    r = np.zeros(n)
+    for j0 in range(0, n, bc):
+        j1 = min(j0 + bc, n)
+        for i0 in range(0, n, br):
+            i1 = min(i0 + br, n)
+            if causal and j0 > i1 - 1:
+                continue
+            s = (q[i0:i1] @ k[j0:j1].T) * sc
+            if causal:
+                s = np.where(causal_mask(i0, i1 - i0, j1 - j0, k_start=j0), NEG_INF, s)
+            m_t = s.max(axis=1)
+            seen = np.isfinite(m_t)  # rows with a visible key in this block
+            p_t = np.where(seen[:, None], np.exp(s - np.where(seen, m_t, 0.0)[:, None]), 0.0)
+            r_t = p_t.sum(axis=1)
+            m_old, r_old = m[i0:i1], r[i0:i1]
+            m_new = np.maximum(m_old, m_t)
+            fin_new = np.isfinite(m_new)
+            base = np.where(fin_new, m_new, 0.0)
+            conv_old = np.where(np.isfinite(m_old), np.exp(np.where(np.isfinite(m_old), m_old, 0.0) - base), 0.0)
+            conv_new = np.where(seen, np.exp(np.where(seen, m_t, 0.0) - base), 0.0)
+            r_new = conv_old * r_old + conv_new * r_t
+            safe = np.where(r_new > 0, r_new, 1.0)
+            c = np.where(r_new > 0, conv_old * r_old / safe, 0.0)
+            pour = conv_new[:, None] * (p_t @ v[j0:j1]) / safe[:, None]
+            out[i0:i1] = c[:, None] * out[i0:i1] + pour
+            m[i0:i1], r[i0:i1] = m_new, r_new
+    return out, m + np.log(r)
 
 
 def io_flash(n: int, d: int, br: int, kv_cached: bool = False) -> float:

@@ -81,6 +81,13 @@ def _pins_pass(o) -> bool:
                 rows = np.array([min(br, 11 - a * br) for a in range(computed.shape[0])])
                 assert sb["dq_atomic_adds"] == int((computed.sum(axis=1) * rows).sum()) * 4
         assert o.io_flash(8, 2, 4) == 104 and o.io_flash(8, 2, 4, kv_cached=True) == 72
+        # the key-major loop order (first algorithm)
+        for causal in (False, True):
+            d_o, d_l = o.attention_dense(qb, kb, vb, causal=causal)
+            for br, bc in ((2, 3), (4, 4)):
+                k_o, k_l = o.attention_fa1_keymajor(qb, kb, vb, br, bc, causal=causal)
+                np.testing.assert_allclose(k_o, d_o, atol=1e-12)
+                np.testing.assert_allclose(k_l, d_l, atol=1e-12)
         # a query block at the end of a square causal problem (general q_start)
         qs_o, qs_l = o.attention_dense(qb[7:], kb, vb, causal=True, q_start=7)
         sq_o, sq_l = o.attention_dense(qb, kb, vb, causal=True)
@@ -129,6 +136,9 @@ MUTATIONS = [
     ("blocked backward: D term dropped", "ds = p * (dp - row_dot[i0:i1, None])", "ds = p * dp"),
     ("blocked backward: dq adds miss rows", "(i1 - i0) * q.shape[1])", "q.shape[1])"),
     ("io_flash: K and V always cached", "(1 if kv_cached else -(-n // br))", "1"),
+    ("key-major: old sum not repaired", "r_new = conv_old * r_old + conv_new * r_t", "r_new = r_old + conv_new * r_t"),
+    ("key-major: blend not diluted", "c = np.where(r_new > 0, conv_old * r_old / safe, 0.0)", "c = np.where(r_new > 0, conv_old, 0.0)"),
+    ("key-major: newcomer not converted", "pour = conv_new[:, None] * (p_t @ v[j0:j1]) / safe[:, None]", "pour = (p_t @ v[j0:j1]) / safe[:, None]"),
     ("mask ignores q_start", "qpos = np.arange(q_start, q_start + nq)[:, None]", "qpos = np.arange(0, nq)[:, None]"),
     ("dense backward ignores q_start", "_, _, p = _dense_rows(q_rows, k[h], v[h], sc, causal, q_start + r0)",
      "_, _, p = _dense_rows(q_rows, k[h], v[h], sc, causal, r0)"),
