@@ -488,7 +488,7 @@ def run_all_workloads(reps):
     with CUDA events (median of `reps`), with L2 flushed by a 256 MB write before
     every timed call, so that small workloads are not timed from a warm L2."""
     from exact_attention_flash_gb300 import (backward_workspace_bytes, decode_auto_split, fa_backward, fa_decode,
-                                             fa_forward, fa_merge_states)
+                                             fa_forward, fa_forward_keymajor, fa_merge_states)
     from exact_attention_flash_gb300.build import build
     from exact_attention_flash_gb300.workloads import WORKLOADS, make_attention_inputs, make_decode_inputs
 
@@ -516,6 +516,13 @@ def run_all_workloads(reps):
     extra[f"decode_b16h32_l32768_d128_auto{n_auto}"] = {"decode": (
         lambda: fa_decode(qa, ka, va, n_auto, out=oa, lse=la),  # noqa: E731
         decode_bytes(wd.B, wd.H, wd.N, wd.d, n_auto), "GB/s")}
+    # The first algorithm's key-major loop order on the bench's causal workload, for comparison.
+    wk = WORKLOADS["causal_fwdbwd_b2h16_n8192_d128_qk8"]
+    qk_, kk_, vk_, _ = make_attention_inputs(wk.B, wk.H, wk.N, wk.d, wk.seed, "cuda", qk_mult=wk.qk_mult,
+                                              with_do=False)
+    extra["causal_b2h16_n8192_d128_qk8 (key-major order)"] = {"forward_keymajor": (
+        lambda: fa_forward_keymajor(qk_, kk_, vk_, causal=True),  # noqa: E731
+        attention_flops(wk.B, wk.H, wk.N, wk.d, True, False), "TFLOP/s")}
     for name, w in list(WORKLOADS.items()) + list(extra.items()):
         if isinstance(w, dict):
             calls = w

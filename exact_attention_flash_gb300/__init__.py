@@ -15,7 +15,7 @@ from ._lib import FAError
 
 __all__ = ["fa_forward", "fa_backward", "fa_decode", "fa_device_status", "FAError", "backward_workspace_bytes",
            "decode_workspace_bytes", "fa_set_stats", "stats_counters", "STATS_FIELDS", "fa_merge_states",
-           "decode_auto_split"]
+           "decode_auto_split", "fa_forward_keymajor"]
 
 # Order of the counters behind fa_set_stats ("attention_kernels.py" sections 3-4, ``stats``).
 STATS_FIELDS = ("tiles", "skipped", "rescales", "dq_atomic_adds")
@@ -213,4 +213,28 @@ def fa_merge_states(o_a, lse_a, o_b, lse_b, out=None, lse=None, stream=None):
                                lse.data_ptr(), _lib.FA_F32 if o_a.dtype == torch.float32 else _lib.FA_BF16,
                                lse_a.numel(), d, _stream_ptr(stream))
     _lib.check("fa_merge_states", code)
+    return out, lse
+
+
+def fa_forward_keymajor(q, k, v, causal=False, scale=None, out_dtype=torch.bfloat16, workspace=None, stream=None):
+    """O, LSE as :func:`fa_forward` gives them, computed in the first algorithm's key-major loop order.
+
+    For comparison only: one CTA per (batch, head), much slower than fa_forward.
+    q, k, v [B, H, N, d] bf16.
+    """
+    lib = _lib.load()
+    _check_bf16("q", q)
+    B, H, N, d = q.shape
+    _check_bf16("k", k, q.shape)
+    _check_bf16("v", v, q.shape)
+    out = torch.empty((B, H, N, d), device=q.device, dtype=out_dtype)
+    lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    nbytes = int(lib.fa_forward_keymajor_workspace_size(B, H, N, d))
+    if workspace is None:
+        workspace = torch.empty(nbytes, device=q.device, dtype=torch.uint8)
+    code = lib.fa_forward_keymajor(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                   _lib.FA_F32 if out.dtype == torch.float32 else _lib.FA_BF16, lse.data_ptr(),
+                                   B, H, N, d, _scale_arg(scale), int(bool(causal)), workspace.data_ptr(),
+                                   workspace.numel(), _stream_ptr(stream))
+    _lib.check("fa_forward_keymajor", code)
     return out, lse

@@ -41,6 +41,8 @@ SIGNATURES = {
     "fa_device_status": (_I, [_P]),
     "fa_set_stats": (_I, [_P]),
     "fa_merge_states": (_I, [_P, _P, _P, _P, _P, _P, _I, ctypes.c_longlong, _I, _P]),
+    "fa_forward_keymajor_workspace_size": (_Z, [_I, _I, _I, _I]),
+    "fa_forward_keymajor": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
     "fa_decode_auto_split": (_I, [_I, _I, _I]),
     "fa_debug_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
 }

@@ -240,13 +240,52 @@ fa_status fa_decode(const void* q, const void* k, const void* v, float* o, float
   return fa::launch_decode(a, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+size_t fa_forward_keymajor_workspace_size(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  return round_up(rows * d * sizeof(float), 256) + 2 * round_up(rows * sizeof(float), 256);
+}
+
+fa_status fa_forward_keymajor(const void* q, const void* k, const void* v, void* o, fa_dtype o_dtype, float* lse,
+                              int B, int H, int N, int d, float scale, int causal, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+  if (o_dtype != FA_BF16 && o_dtype != FA_F32) return FA_ERR_INVALID_ARG;
+  fa_status st = check_common(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < fa_forward_keymajor_workspace_size(B, H, N, d))
+    return FA_ERR_WORKSPACE;
+  fa::KeyMajorArgs a{};
+  const int BH = B * H;
+  if ((st = make_row_tile_map(&a.tm_q, q, BH, N, d)) != FA_OK) return st;
+  if ((st = make_row_tile_map(&a.tm_k, k, BH, N, d)) != FA_OK) return st;
+  if ((st = make_row_tile_map(&a.tm_v, v, BH, N, d)) != FA_OK) return st;
+  const size_t rows = static_cast<size_t>(BH) * N;
+  char* ws = static_cast<char*>(workspace);
+  a.ws_o = reinterpret_cast<float*>(ws);
+  a.ws_m = reinterpret_cast<float*>(ws + round_up(rows * d * sizeof(float), 256));
+  a.ws_r = reinterpret_cast<float*>(ws + round_up(rows * d * sizeof(float), 256) + round_up(rows * sizeof(float), 256));
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.d = d;
+  a.scale_log2 = resolve_scale(scale, d) * kLog2e;
+  a.causal = causal ? 1 : 0;
+  a.o_f32 = (o_dtype == FA_F32) ? 1 : 0;
+  return fa::launch_forward_keymajor(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 fa_status fa_device_status(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  unsigned f = 0, b = 0, dcd = 0;
+  unsigned f = 0, b = 0, dcd = 0, km = 0;
   if (fa::read_clear_forward_status(&f, s) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::read_clear_backward_status(&b, s) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::read_clear_decode_status(&dcd, s) != cudaSuccess) return FA_ERR_CUDA;
-  const unsigned all = f | b | dcd;
+  if (fa::read_clear_keymajor_status(&km, s) != cudaSuccess) return FA_ERR_CUDA;
+  const unsigned all = f | b | dcd | km;
   if (all & 1u) return FA_ERR_TIMEOUT;
   if (all != 0u) return FA_ERR_CUDA;
   return FA_OK;

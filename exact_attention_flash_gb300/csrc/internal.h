@@ -73,10 +73,25 @@ struct DecodeArgs {
   float scale_log2;
 };
 
+// The first algorithm's loop order (fa_fwd_keymajor.cu): square case only.
+struct KeyMajorArgs {
+  CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps over [B*H, N, d] bf16, box {64, 128, 1}, 128B swizzle
+  void* o;                       // [B, H, N, d] bf16 or fp32
+  float* lse;                    // [B, H, N]
+  float* ws_o;                   // workspace: running O [B*H, N, d] fp32
+  float* ws_m;                   // running max (log2 units) [B*H, N]
+  float* ws_r;                   // running sum [B*H, N]
+  int B, H, N, d;
+  float scale_log2;
+  int causal;
+  int o_f32;
+};
+
 // Each returns a cudaError_t from the launch (cudaSuccess when queued).
 cudaError_t launch_forward(const ForwardArgs& a, cudaStream_t stream);
 cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_forward_keymajor(const KeyMajorArgs& a, cudaStream_t stream);
 
 // Merge of two (O, LSE) results over disjoint key sets (fa_merge.cu); o_f32: O is
 // fp32, else bf16.  O rows of d elements, d a multiple of 4.
@@ -90,6 +105,7 @@ int decode_auto_split(int BH, int L, int sms);
 cudaError_t read_clear_forward_status(unsigned* out, cudaStream_t stream);
 cudaError_t read_clear_backward_status(unsigned* out, cudaStream_t stream);
 cudaError_t read_clear_decode_status(unsigned* out, cudaStream_t stream);
+cudaError_t read_clear_keymajor_status(unsigned* out, cudaStream_t stream);
 
 // Test hook: one CTA waits on an mbarrier that nothing completes, with the
 // given limit in nanoseconds; it must come back with the timeout bit set.

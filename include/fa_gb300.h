@@ -210,6 +210,31 @@ fa_status fa_decode_noalloc(const void* q, const void* k, const void* v, float* 
  */
 fa_status fa_device_status(void* stream);
 
+/* Bytes of workspace fa_forward_keymajor needs: the running O (fp32), maximum and
+ * sum of every query row. */
+size_t fa_forward_keymajor_workspace_size(int B, int H, int N, int d);
+
+/*
+ * fa_forward_keymajor — the forward in the first algorithm's loop order, for
+ * comparison with fa_forward.  Same result as fa_forward (O and LSE), by a
+ * different schedule: key tiles outer, query tiles inner, and the running output,
+ * maximum and sum of every query row kept in the workspace and repaired at every
+ * visit, O renormalised each time.
+ *
+ * Defines: "flash_attention_numpy.py" ``flash_attention_tier1`` (key blocks
+ * outer, query blocks inner; r' = e^(m - m') r + e^(m~ - m') r~,
+ * O = (e^(m - m') r / r') O + e^(m~ - m') (p~ V_j) / r'), with the scale and the
+ * causal skip and mask of "attention_kernels.py" section 3.  Blocks are 128 x 128.
+ * One CTA per (batch, head) and no overlap between the steps of a visit: it
+ * shows the loop order, and is much slower than fa_forward.
+ *
+ * Arguments as for fa_forward (no precise mode), plus a workspace of
+ * >= fa_forward_keymajor_workspace_size() bytes, 16-byte aligned.
+ */
+fa_status fa_forward_keymajor(const void* q, const void* k, const void* v, void* o, fa_dtype o_dtype, float* lse,
+                              int B, int H, int N, int d, float scale, int causal, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
 /*
  * fa_merge_states — combines two attention results over disjoint key sets.
  *

@@ -108,6 +108,16 @@ def test_merge_and_auto_split_reject_bad_arguments(lib):
     assert lib.fa_decode_auto_split(1, 1, 0) == 0
 
 
+def test_keymajor_workspace_and_arguments(lib):
+    rows = 2 * 3 * 100
+    assert lib.fa_forward_keymajor_workspace_size(2, 3, 100, 128) == ((rows * 128 * 4 + 255) // 256 + 2 * ((rows * 4 + 255) // 256)) * 256
+    assert lib.fa_forward_keymajor_workspace_size(0, 3, 100, 128) == 0
+    # (q, k, v, o, o_dtype, lse, B, H, N, d, scale, causal, workspace, bytes, stream)
+    assert lib.fa_forward_keymajor(None, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 64, 0.0, 0, FAKE, 1 << 20, None) == 1
+    assert lib.fa_forward_keymajor(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 48, 0.0, 0, FAKE, 1 << 20, None) == 2
+    assert lib.fa_forward_keymajor(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 64, 0.0, 0, FAKE, 16, None) == 5
+
+
 def test_set_stats_arguments(lib):
     # the counters must be 8-byte aligned; NULL stops counting (nothing runs here)
     assert lib.fa_set_stats(FAKE + 4) == 1
