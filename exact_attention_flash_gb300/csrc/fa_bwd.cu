@@ -511,13 +511,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         for (int kq = 0; kq < 8; ++kq) {
           const float x0 = __uint_as_float(v[4 * kq]) * a.scale, x1 = __uint_as_float(v[4 * kq + 1]) * a.scale;
           const float x2 = __uint_as_float(v[4 * kq + 2]) * a.scale, x3 = __uint_as_float(v[4 * kq + 3]) * a.scale;
-          // Round 1 (lanes i, i ^ 1): even lanes keep queries 0 and 2, odd lanes 1 and 3,
+          // Exchange 1 (lanes i, i ^ 1): even lanes keep queries 0 and 2, odd lanes 1 and 3,
           // each for both features of the pair.
           const bool odd = i4 & 1;
           const float r0 = __shfl_xor_sync(0xffffffffu, odd ? x0 : x1, 1);
           const float r1 = __shfl_xor_sync(0xffffffffu, odd ? x2 : x3, 1);
           const float a0 = odd ? r0 : x0, a1 = odd ? x1 : r0, a2 = odd ? r1 : x2, a3 = odd ? x3 : r1;
-          // Round 2 (lanes i, i ^ 2): exchange the other feature pair.
+          // Exchange 2 (lanes i, i ^ 2): swap the other feature pair.
           const bool hi = i4 & 2;
           const float t0 = __shfl_xor_sync(0xffffffffu, hi ? a0 : a2, 2);
           const float t1 = __shfl_xor_sync(0xffffffffu, hi ? a1 : a3, 2);
