@@ -5,11 +5,13 @@
 // ``flash_backward``; "lab.py" ``backward``): D = rowsum(dO * O); for each key
 // tile j and query tile i, S = Q_i K_j^T * scale, P = exp(S - L_i),
 // dV_j += P^T dO_i, dP = dO_i V_j^T, dS = P * (dP - D_i),
-// dQ_i += dS K_j * scale, dK_j += dS^T Q_i * scale.  Causal: query tiles that
-// lie wholly before the key tile are skipped; the others are masked per element.
+// dQ_i += dS K_j * scale, dK_j += dS^T Q_i * scale.  Causal (query i at position
+// q_start + i sees key j iff j <= q_start + i): query tiles that lie wholly before
+// the key tile are skipped, the others are masked per element, and a key tile that
+// no query sees gets zero dK and dV.
 //
 // Kernels:
-//   bwd_preprocess  one warp per row: D = rowsum(dO * O), the per-query biases
+//   bwd_preprocess  D/8 lanes per row: D = rowsum(dO * O), the per-query biases
 //                   -LSE/scale and -D as tensor-core operand tiles, and dQ := 0.
 //   bwd_kernel      one CTA per (128-key tile, batch*head); it walks the query
 //                   tiles of 64 rows.  Keys are the TMEM lanes, so the kernel

@@ -5,9 +5,10 @@
 // ``flash_forward``; "lab.py" ``tiled``): for each query row, over key tiles,
 // S = Q K^T * scale, m' = max(m, rowmax S), P = exp(S - m'), l = l * exp(m - m')
 // + rowsum P, acc = acc * exp(m - m') + P V, and at the end O = acc / l and
-// L = m + ln l.  Causal: key j is visible to query i iff j <= i; key tiles
-// wholly in the future of a query tile are skipped, and only the diagonal tile
-// is masked.
+// L = m + ln l.  Query row i sits at position q_start + i (0 for self-attention);
+// causal: key j is visible to query i iff j <= q_start + i; key tiles wholly in
+// the future of a query tile are skipped, and only tiles that straddle a row's
+// last visible key are masked.
 //
 // GPU design (one CTA = two 128-row query tiles, 256 rows):
 //   warp 8      TMA producer: both Q tiles once, then K and V tiles of 128 keys
