@@ -341,61 +341,72 @@ def run_ours(args, world, rank, local):
     # each reuse.  The timed region runs from before the first copy in to after the
     # last copy out, so every step's copies are inside it.
     host_in = [t.cpu().pin_memory() for t in (q, k, v, do)]
-    outs = (o, lse, dq, dk, dv)
-    host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs] for _ in range(2)]
     dev_in = [[torch.empty_like(t) for t in (q, k, v, do)] for _ in range(2)]
-    dev_out = [[torch.empty_like(t) for t in outs] for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
     s_in = torch.cuda.Stream(dev)
     s_out = torch.cuda.Stream(dev)
 
-    def e2e_run(steps):
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        start.record(stream)
-        s_in.wait_event(start)
-        s_out.wait_event(start)
-        computed = [None, None]  # compute of the last step that read dev_in[b]
-        copied = [None, None]    # copy out of the last step that wrote dev_out[b]
-        for i in range(steps):
-            b = i % 2
-            if computed[b] is not None:
-                s_in.wait_event(computed[b])
-            with torch.cuda.stream(s_in):
-                for dst, src in zip(dev_in[b], host_in):
-                    dst.copy_(src, non_blocking=True)
-            ev_in = torch.cuda.Event()
-            ev_in.record(s_in)
-            stream.wait_event(ev_in)
-            if copied[b] is not None:
-                stream.wait_event(copied[b])
-            x = dev_in[b]
-            ob, lb, dqb, dkb, dvb = dev_out[b]
-            fa_forward(x[0], x[1], x[2], causal=True, out=ob, lse=lb, stream=stream)
-            fa_backward(x[0], x[1], x[2], ob, lb, x[3], causal=True, workspace=ws_b, dq=dqb, dk=dkb, dv=dvb,
-                        stream=stream)
-            computed[b] = torch.cuda.Event()
-            computed[b].record(stream)
-            s_out.wait_event(computed[b])
-            with torch.cuda.stream(s_out):
-                for dst, src in zip(host_out[b], dev_out[b]):
-                    dst.copy_(src, non_blocking=True)
-            copied[b] = torch.cuda.Event()
-            copied[b].record(s_out)
-        done = torch.cuda.Event()
-        done.record(s_out)
-        stream.wait_event(done)
-        end.record(stream)
-        return start, end
+    def make_e2e(grad_dtype):
+        """The pipelined end-to-end step for gradients of ``grad_dtype``, and its bytes copied out."""
+        ws = ws_b if grad_dtype == torch.float32 else torch.empty(
+            backward_workspace_bytes(w.B, w.H, w.N, w.d, grad_dtype), device=dev, dtype=torch.uint8)
+        outs = (o, lse) + tuple(torch.empty(t.shape, dtype=grad_dtype, device=dev) for t in (dq, dk, dv))
+        host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs] for _ in range(2)]
+        dev_out = [[torch.empty_like(t) for t in outs] for _ in range(2)]
 
-    e2e_run(2)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    e0, e1 = e2e_run(n)
-    torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n, world)
-    e2e_value = world * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12
+        def run(steps):
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            s_in.wait_event(start)
+            s_out.wait_event(start)
+            computed = [None, None]  # compute of the last step that read dev_in[b]
+            copied = [None, None]    # copy out of the last step that wrote dev_out[b]
+            for i in range(steps):
+                b = i % 2
+                if computed[b] is not None:
+                    s_in.wait_event(computed[b])
+                with torch.cuda.stream(s_in):
+                    for dst, src in zip(dev_in[b], host_in):
+                        dst.copy_(src, non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(s_in)
+                stream.wait_event(ev_in)
+                if copied[b] is not None:
+                    stream.wait_event(copied[b])
+                x = dev_in[b]
+                ob, lb, dqb, dkb, dvb = dev_out[b]
+                fa_forward(x[0], x[1], x[2], causal=True, out=ob, lse=lb, stream=stream)
+                fa_backward(x[0], x[1], x[2], ob, lb, x[3], causal=True, workspace=ws, dq=dqb, dk=dkb, dv=dvb,
+                            stream=stream, grad_dtype=grad_dtype)
+                computed[b] = torch.cuda.Event()
+                computed[b].record(stream)
+                s_out.wait_event(computed[b])
+                with torch.cuda.stream(s_out):
+                    for dst, src in zip(host_out[b], dev_out[b]):
+                        dst.copy_(src, non_blocking=True)
+                copied[b] = torch.cuda.Event()
+                copied[b].record(s_out)
+            done = torch.cuda.Event()
+            done.record(s_out)
+            stream.wait_event(done)
+            end.record(stream)
+            return start, end
+
+        return run, sum(t.numel() * t.element_size() for t in host_out[0])
+
+    def e2e_measure(grad_dtype):
+        run, d2h = make_e2e(grad_dtype)
+        run(2)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e0, e1 = run(n)
+        torch.cuda.synchronize(dev)
+        ms = max_over_ranks(e0.elapsed_time(e1) / n, world)
+        return world * (f_fwd + f_bwd) / (ms * 1e-3) / 1e12, d2h
+
+    e2e_value, d2h = e2e_measure(torch.float32)
+    e2e16_value, d2h16 = e2e_measure(torch.bfloat16)
 
     if rank != 0:
         return
@@ -432,7 +443,11 @@ def run_ours(args, world, rank, local):
                        "algorithmic_bytes": dbytes,
                        "traffic": recorded_traffic("fa_decode.cu", "decode_split_kernel_d128")},
         },
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "grad_dtype": "f32"},
+        # the same pipeline with the gradients returned as bf16 (fp32 accumulation inside)
+        "e2e_bf16_grads": {"value": e2e16_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                           "d2h_bytes_per_step": d2h16},
         "gpu_launches": 4 * n,
         "clocks": clocks,
         "cpu_baseline": cpu,
@@ -545,6 +560,12 @@ def run_all_workloads(reps):
                 ws = torch.empty(backward_workspace_bytes(w.B, w.H, w.N, w.d), device="cuda", dtype=torch.uint8)
                 calls["backward"] = (lambda: fa_backward(q, k, v, o, lse, do, causal=w.causal, workspace=ws),  # noqa: E731
                                      attention_flops(w.B, w.H, w.N, w.d, w.causal, True), "TFLOP/s")
+                ws16 = torch.empty(backward_workspace_bytes(w.B, w.H, w.N, w.d, torch.bfloat16), device="cuda",
+                                   dtype=torch.uint8)
+                calls["backward (bf16 gradients)"] = (
+                    lambda: fa_backward(q, k, v, o, lse, do, causal=w.causal, workspace=ws16,  # noqa: E731
+                                        grad_dtype=torch.bfloat16),
+                    attention_flops(w.B, w.H, w.N, w.d, w.causal, True), "TFLOP/s")
         _time_calls(name, calls, reps, flush, e0, e1, peaks)
         del calls
         torch.cuda.empty_cache()

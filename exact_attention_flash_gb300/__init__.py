@@ -72,19 +72,30 @@ def fa_forward(q, k, v, causal=False, scale=None, out_dtype=torch.bfloat16, prec
     return out, lse
 
 
-def backward_workspace_bytes(B, H, N, d) -> int:
-    """Workspace of fa_backward for N (= Nq) query rows."""
-    return int(_lib.load().fa_backward_workspace_size(B, H, N, d))
+def backward_workspace_bytes(B, H, N, d, grad_dtype=torch.float32) -> int:
+    """Workspace bytes of :func:`fa_backward` (N = Nq) for gradients of ``grad_dtype``."""
+    return int(_lib.load().fa_backward_workspace_size(B, H, N, d, _grad_code(grad_dtype)))
+
+
+def _grad_code(grad_dtype):
+    if grad_dtype == torch.float32:
+        return _lib.FA_F32
+    if grad_dtype == torch.bfloat16:
+        return _lib.FA_BF16
+    raise ValueError("grad_dtype must be torch.float32 or torch.bfloat16")
 
 
 def fa_backward(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, dk=None, dv=None,
-                stream=None, q_start=0):
-    """dQ, dK, dV (fp32) of sum(O * dO) by recomputation from LSE.
+                stream=None, q_start=0, grad_dtype=torch.float32):
+    """dQ, dK, dV of sum(O * dO) by recomputation from LSE.
 
     Shapes as for :func:`fa_forward` (q, o, do [B, H, Nq, d]; k, v [B, H, Nk, d];
-    lse [B, H, Nq]); causal, scale and q_start must match the forward call.
+    lse [B, H, Nq]); causal, scale and q_start must match the forward call.  The
+    products accumulate in fp32; ``grad_dtype`` (fp32 or bf16) is the type of the
+    returned gradients.
     """
     lib = _lib.load()
+    g_code = _grad_code(grad_dtype)
     _check_bf16("q", q)
     B, H, Nq, d = q.shape
     if k.dim() != 4:
@@ -95,20 +106,20 @@ def fa_backward(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, d
     _check_bf16("do", do, q.shape)
     _check_out("o", o, q.shape, (torch.bfloat16, torch.float32))
     _check_out("lse", lse, (B, H, Nq), (torch.float32,))
-    nbytes = backward_workspace_bytes(B, H, Nq, d)
+    nbytes = backward_workspace_bytes(B, H, Nq, d, grad_dtype)
     if workspace is None:
         workspace = torch.empty(nbytes, device=q.device, dtype=torch.uint8)
-    dq = torch.empty((B, H, Nq, d), device=q.device, dtype=torch.float32) if dq is None else dq
-    dk = torch.empty((B, H, Nk, d), device=q.device, dtype=torch.float32) if dk is None else dk
-    dv = torch.empty((B, H, Nk, d), device=q.device, dtype=torch.float32) if dv is None else dv
-    _check_out("dq", dq, (B, H, Nq, d), (torch.float32,))
-    _check_out("dk", dk, (B, H, Nk, d), (torch.float32,))
-    _check_out("dv", dv, (B, H, Nk, d), (torch.float32,))
+    dq = torch.empty((B, H, Nq, d), device=q.device, dtype=grad_dtype) if dq is None else dq
+    dk = torch.empty((B, H, Nk, d), device=q.device, dtype=grad_dtype) if dk is None else dk
+    dv = torch.empty((B, H, Nk, d), device=q.device, dtype=grad_dtype) if dv is None else dv
+    _check_out("dq", dq, (B, H, Nq, d), (grad_dtype,))
+    _check_out("dk", dk, (B, H, Nk, d), (grad_dtype,))
+    _check_out("dv", dv, (B, H, Nk, d), (grad_dtype,))
     o_code = _lib.FA_F32 if o.dtype == torch.float32 else _lib.FA_BF16
     code = lib.fa_backward_qk(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), o_code, lse.data_ptr(),
-                              do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, int(q_start), d,
-                              _scale_arg(scale), int(bool(causal)), workspace.data_ptr(), workspace.numel(),
-                              _stream_ptr(stream))
+                              do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), g_code, B, H, Nq, Nk,
+                              int(q_start), d, _scale_arg(scale), int(bool(causal)), workspace.data_ptr(),
+                              workspace.numel(), _stream_ptr(stream))
     _lib.check("fa_backward_qk", code)
     return dq, dk, dv
 

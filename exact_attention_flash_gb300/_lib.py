@@ -32,9 +32,9 @@ SIGNATURES = {
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_forward": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _F, _I, _I, _P]),
     "fa_forward_qk": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
-    "fa_backward_workspace_size": (_Z, [_I, _I, _I, _I]),
-    "fa_backward_qk": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
-    "fa_backward": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
+    "fa_backward_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "fa_backward_qk": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
+    "fa_backward": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
     "fa_decode_workspace_size": (_Z, [_I, _I, _I, _I]),
     "fa_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _Z, _P]),
     "fa_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),

@@ -43,17 +43,19 @@ fa_status make_row_tile_map(CUtensorMap* m, const void* ptr, int BH, int N, int 
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-// dK or dV [B*H, N, d] fp32 as a 3-D tensor, tiles of 128 rows x 32 features with the
-// 128-byte swizzle: the backward stores each key tile's gradients with bulk tensor
-// stores; rows past N are dropped.
-fa_status make_grad_store_map(CUtensorMap* m, void* ptr, int BH, int N, int d) {
+// dK or dV [B*H, N, d] as a 3-D tensor, tiles of 128 rows x 128 bytes (32 fp32 or 64
+// bf16 features) with the 128-byte swizzle: the backward stores each key tile's
+// gradients with bulk tensor stores; rows past N are dropped.
+fa_status make_grad_store_map(CUtensorMap* m, void* ptr, int BH, int N, int d, bool bf16) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return FA_ERR_CUDA;
+  const cuuint64_t esize = bf16 ? 2 : 4;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4};
-  const cuuint32_t box[3] = {32, 128, 1};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * esize, static_cast<cuuint64_t>(N) * d * esize};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esize), 128, 1};
   const cuuint32_t elem[3] = {1, 1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, elem,
+  const CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims,
+                         strides, box, elem,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
@@ -82,6 +84,11 @@ float resolve_scale(float scale, int d) { return scale > 0.f ? scale : 1.0f / st
 constexpr float kLog2e = 1.4426950408889634f;
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Backward workspace: the bias tiles, then (bf16 gradients) the fp32 dQ accumulator.
+size_t backward_bias_bytes(int B, int H, int N) {
+  return static_cast<size_t>(B) * H * round_up(static_cast<size_t>(N), 64) * 64;
+}
 
 // Counters set by fa_set_stats for the calling host thread's calls (null: none).
 thread_local unsigned long long* t_stats = nullptr;
@@ -140,48 +147,56 @@ fa_status fa_forward_qk(const void* q, const void* k, const void* v, void* o, fa
 }
 
 // Per query row over [B*H, N rounded up to 64]: two 32-byte rows of the bias tiles
-// (-LSE/scale and -D as three bf16 terms each).
-size_t fa_backward_workspace_size(int B, int H, int N, int d) {
-  (void)d;
-  if (B < 1 || H < 1 || N < 1) return 0;
-  const size_t n_pad = round_up(static_cast<size_t>(N), 64);
-  return static_cast<size_t>(B) * H * n_pad * 64;
+// (-LSE/scale and -D as three bf16 terms each); for bf16 gradients then, at a 256-byte
+// boundary, the fp32 dQ accumulator [B, H, N, d].
+size_t fa_backward_workspace_size(int B, int H, int N, int d, fa_dtype grad_dtype) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+  if (grad_dtype == FA_F32) return backward_bias_bytes(B, H, N);
+  if (grad_dtype != FA_BF16) return 0;
+  return round_up(backward_bias_bytes(B, H, N), 256) + static_cast<size_t>(B) * H * N * d * sizeof(float);
 }
 
 fa_status fa_backward(const void* q, const void* k, const void* v, const void* o, fa_dtype o_dtype,
-                      const float* lse, const void* dout, float* dq, float* dk, float* dv, int B, int H, int N, int d,
-                      float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
-  return fa_backward_qk(q, k, v, o, o_dtype, lse, dout, dq, dk, dv, B, H, N, N, 0, d, scale, causal, workspace,
-                        workspace_bytes, stream);
+                      const float* lse, const void* dout, void* dq, void* dk, void* dv, fa_dtype grad_dtype, int B,
+                      int H, int N, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  return fa_backward_qk(q, k, v, o, o_dtype, lse, dout, dq, dk, dv, grad_dtype, B, H, N, N, 0, d, scale, causal,
+                        workspace, workspace_bytes, stream);
 }
 
 fa_status fa_backward_qk(const void* q, const void* k, const void* v, const void* o, fa_dtype o_dtype,
-                         const float* lse, const void* dout, float* dq, float* dk, float* dv, int B, int H, int Nq,
-                         int Nk, int q_start, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
-                         void* stream) {
+                         const float* lse, const void* dout, void* dq, void* dk, void* dv, fa_dtype grad_dtype, int B,
+                         int H, int Nq, int Nk, int q_start, int d, float scale, int causal, void* workspace,
+                         size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
       !aligned16(dk) || !aligned16(dv))
     return FA_ERR_INVALID_ARG;
   if (o_dtype != FA_BF16 && o_dtype != FA_F32) return FA_ERR_INVALID_ARG;
+  if (grad_dtype != FA_BF16 && grad_dtype != FA_F32) return FA_ERR_INVALID_ARG;
   fa_status st = check_lengths(B, H, Nq, Nk, q_start, d);
   if (st != FA_OK) return st;
-  if (!workspace || !aligned16(workspace) || workspace_bytes < fa_backward_workspace_size(B, H, Nq, d))
+  if (!workspace || !aligned16(workspace) || workspace_bytes < fa_backward_workspace_size(B, H, Nq, d, grad_dtype))
     return FA_ERR_WORKSPACE;
+  const bool grad_bf16 = grad_dtype == FA_BF16;
   fa::BackwardArgs a{};
   const int BH = B * H;
   if ((st = make_row_tile_map(&a.tm_q, q, BH, Nq, d, 64)) != FA_OK) return st;
   if ((st = make_row_tile_map(&a.tm_k, k, BH, Nk, d, 128)) != FA_OK) return st;
   if ((st = make_row_tile_map(&a.tm_v, v, BH, Nk, d, 128)) != FA_OK) return st;
   if ((st = make_row_tile_map(&a.tm_do, dout, BH, Nq, d, 64)) != FA_OK) return st;
-  if ((st = make_grad_store_map(&a.tm_dk, dk, BH, Nk, d)) != FA_OK) return st;
-  if ((st = make_grad_store_map(&a.tm_dv, dv, BH, Nk, d)) != FA_OK) return st;
+  if ((st = make_grad_store_map(&a.tm_dk, dk, BH, Nk, d, grad_bf16)) != FA_OK) return st;
+  if ((st = make_grad_store_map(&a.tm_dv, dv, BH, Nk, d, grad_bf16)) != FA_OK) return st;
   a.o = o;
   a.dout = dout;
   a.lse = lse;
-  a.dq = dq;
+  a.dq = grad_bf16 ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                              round_up(backward_bias_bytes(B, H, Nq), 256))
+                   : static_cast<float*>(dq);
+  a.dq_out = dq;
   a.dk = dk;
   a.dv = dv;
+  a.grad_bf16 = grad_bf16 ? 1 : 0;
   a.n_pad = static_cast<int>(round_up(static_cast<size_t>(Nq), 64));
   a.bias = static_cast<uint8_t*>(workspace);
   a.B = B;

@@ -31,6 +31,8 @@
 //   lands in the dP^T buffer that dS^T of step n has just left.
 // Tensor memory (512 columns): S^T[2] [0,64) [64,128), dP^T[2] [128,192)
 // [192,256), dV [256, 256+d), dK [256+d, 256+2d).
+// Gradients leave as fp32, or as bf16: the epilogue rounds dK and dV, and dQ is
+// accumulated in an fp32 workspace buffer that dq_to_bf16 rounds after the grid.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -154,11 +156,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     // No query sees these keys (they lie after the last query's position): their
     // gradients are zero.  Nothing else runs in this CTA.
     const int rows = min(kBKV, a.Nk - key0);
-    float4* dk4 = reinterpret_cast<float4*>(a.dk + (static_cast<size_t>(bh) * a.Nk + key0) * D);
-    float4* dv4 = reinterpret_cast<float4*>(a.dv + (static_cast<size_t>(bh) * a.Nk + key0) * D);
-    for (int i = tid; i < rows * (D / 4); i += kBwdThreads) {
-      dk4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      dv4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int row_bytes = D * (a.grad_bf16 ? 2 : 4);
+    const size_t off = (static_cast<size_t>(bh) * a.Nk + key0) * row_bytes;
+    uint4* dk4 = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.dk) + off);
+    uint4* dv4 = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.dv) + off);
+    for (int i = tid; i < rows * row_bytes / 16; i += kBwdThreads) {
+      dk4[i] = make_uint4(0u, 0u, 0u, 0u);
+      dv4[i] = make_uint4(0u, 0u, 0u, 0u);
     }
     return;
   }
@@ -443,38 +447,61 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     }
     // ------------------------------------------------------------ dK, dV epilogue
     // Once the last products are done, the Q/dO/dS buffers are free: dK and dV are
-    // staged there as [128 keys x 32 features] fp32 boxes with the 128-byte swizzle
-    // (16-byte piece j of row k at (j ^ (k % 8)) * 16, so that the staging stores
-    // spread over all banks) and leave with bulk tensor stores, one box per 32
-    // features.  Warpgroup h handles features [h d/2, (h + 1) d/2).
+    // staged there as boxes of 128 keys x 128 bytes (32 fp32 or 64 bf16 features)
+    // with the 128-byte swizzle (16-byte piece j of row k at (j ^ (k % 8)) * 16, so
+    // that the staging stores spread over all banks) and leave with bulk tensor
+    // stores, one per box.  Warpgroup h handles features [h d/2, (h + 1) d/2).
+    constexpr int kBoxBytes = kBKV * 128;  // 16 KB
+    const int box_cols = a.grad_bf16 ? 64 : 32;  // features per box
+    const int n_boxes = D / box_cols;            // per tensor
     const bool e_ok = ok && __all_sync(0xffffffffu, mbar_wait(&sh.dkdv_full, 0, &sh.abort, &g_bwd_status));
     if (e_ok) {
       tc_fence_after();
-      constexpr int kBoxBytes = kBKV * 32 * 4;  // 16 KB
       uint8_t* stage_v = sQ;                        // boxes of dV, then of dK
-      uint8_t* stage_k = sQ + (D / 32) * kBoxBytes;
+      uint8_t* stage_k = sQ + n_boxes * kBoxBytes;
 #pragma unroll 1
       for (int c = h * (D / 2); c < (h + 1) * (D / 2); c += 32) {
         uint32_t uv[32], uk[32];
         tmem_ld32(tmem_addr(tmem, lane_base, C::kDVCol + c), uv);
         tmem_ld32(tmem_addr(tmem, lane_base, C::kDKCol + c), uk);
-        uint8_t* rv = stage_v + (c / 32) * kBoxBytes + k * 128;
-        uint8_t* rk = stage_k + (c / 32) * kBoxBytes + k * 128;
+        uint8_t* rv = stage_v + (c / box_cols) * kBoxBytes + k * 128;
+        uint8_t* rk = stage_k + (c / box_cols) * kBoxBytes + k * 128;
+        if (a.grad_bf16) {
+          // 32 features = 64 bytes: pieces (c % 64) / 8 .. + 3 of the row
+          const int j0 = (c % 64) / 8;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          *reinterpret_cast<uint4*>(rv + ((j ^ (k & 7)) << 4)) = make_uint4(uv[4 * j], uv[4 * j + 1], uv[4 * j + 2], uv[4 * j + 3]);
-          *reinterpret_cast<float4*>(rk + ((j ^ (k & 7)) << 4)) =
-              make_float4(__uint_as_float(uk[4 * j]) * a.scale, __uint_as_float(uk[4 * j + 1]) * a.scale,
-                          __uint_as_float(uk[4 * j + 2]) * a.scale, __uint_as_float(uk[4 * j + 3]) * a.scale);
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t* w = uv + 8 * j;
+            const uint32_t* x = uk + 8 * j;
+            const float s = a.scale;
+            *reinterpret_cast<uint4*>(rv + (((j0 + j) ^ (k & 7)) << 4)) =
+                make_uint4(pack_bf16(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                           pack_bf16(__uint_as_float(w[2]), __uint_as_float(w[3])),
+                           pack_bf16(__uint_as_float(w[4]), __uint_as_float(w[5])),
+                           pack_bf16(__uint_as_float(w[6]), __uint_as_float(w[7])));
+            *reinterpret_cast<uint4*>(rk + (((j0 + j) ^ (k & 7)) << 4)) =
+                make_uint4(pack_bf16(__uint_as_float(x[0]) * s, __uint_as_float(x[1]) * s),
+                           pack_bf16(__uint_as_float(x[2]) * s, __uint_as_float(x[3]) * s),
+                           pack_bf16(__uint_as_float(x[4]) * s, __uint_as_float(x[5]) * s),
+                           pack_bf16(__uint_as_float(x[6]) * s, __uint_as_float(x[7]) * s));
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            *reinterpret_cast<uint4*>(rv + ((j ^ (k & 7)) << 4)) = make_uint4(uv[4 * j], uv[4 * j + 1], uv[4 * j + 2], uv[4 * j + 3]);
+            *reinterpret_cast<float4*>(rk + ((j ^ (k & 7)) << 4)) =
+                make_float4(__uint_as_float(uk[4 * j]) * a.scale, __uint_as_float(uk[4 * j + 1]) * a.scale,
+                            __uint_as_float(uk[4 * j + 2]) * a.scale, __uint_as_float(uk[4 * j + 3]) * a.scale);
+          }
         }
       }
       fence_proxy_async_smem();
     }
     compute_bar_sync();  // all boxes staged (or, after a failed wait, none)
     if (e_ok && tid == 0) {
-      for (int i = 0; i < D / 32; ++i) {
-        tma_store_3d(&a.tm_dv, sQ + i * (kBKV * 32 * 4), 32 * i, key0, bh);
-        tma_store_3d(&a.tm_dk, sQ + (D / 32 + i) * (kBKV * 32 * 4), 32 * i, key0, bh);
+      for (int i = 0; i < n_boxes; ++i) {
+        tma_store_3d(&a.tm_dv, sQ + i * kBoxBytes, box_cols * i, key0, bh);
+        tma_store_3d(&a.tm_dk, sQ + (n_boxes + i) * kBoxBytes, box_cols * i, key0, bh);
       }
       asm volatile("cp.async.bulk.commit_group;" ::: "memory");
       asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -621,6 +648,17 @@ __global__ void __launch_bounds__(256) bwd_preprocess(const void* __restrict__ o
   }
 }
 
+// dQ for bf16 gradients: the fp32 accumulator rounded to bf16, 8 elements per thread
+// and pass (two 16-byte loads, one 16-byte store).
+__global__ void __launch_bounds__(256) dq_to_bf16(const float* __restrict__ src, uint4* __restrict__ dst, long long n8) {
+  const float4* s4 = reinterpret_cast<const float4*>(src);
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float4 a = s4[2 * i], b = s4[2 * i + 1];
+    dst[i] = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
+  }
+}
+
 template <int D>
 cudaError_t launch_bwd_t(const BackwardArgs& a, cudaStream_t stream) {
   using C = BwdCfg<D>;
@@ -654,7 +692,16 @@ cudaError_t launch_bwd_t(const BackwardArgs& a, cudaStream_t stream) {
   attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr_pdl;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, bwd_kernel<D>, a);
+  e = cudaLaunchKernelEx(&cfg, bwd_kernel<D>, a);
+  if (e != cudaSuccess || !a.grad_bf16) return e;
+  // bf16 gradients: dQ leaves its fp32 accumulator once every key tile has added to it.
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const long long n8 = static_cast<long long>(a.B) * a.H * a.Nq * (D / 8);
+  const long long blocks = (n8 + 255) / 256, cap = 8LL * sms;
+  dq_to_bf16<<<static_cast<unsigned>(blocks < cap ? blocks : cap), 256, 0, stream>>>(a.dq, static_cast<uint4*>(a.dq_out), n8);
+  return cudaGetLastError();
 }
 
 }  // namespace

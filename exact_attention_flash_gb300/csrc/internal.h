@@ -25,13 +25,17 @@ struct ForwardArgs {
 
 struct BackwardArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 3-D maps over [B*H, Nq or Nk, d] bf16; Q, dO boxes of 64 rows, K, V of 128
-  CUtensorMap tm_dk, tm_dv;             // 3-D maps over dK, dV [B*H, Nk, d] fp32, box {32, 128, 1}, 128B swizzle
+  CUtensorMap tm_dk, tm_dv;             // 3-D maps over dK, dV [B*H, Nk, d], boxes of 128 rows x 128 bytes
+                                        // ({32, 128, 1} fp32 or {64, 128, 1} bf16), 128B swizzle
   const void* o;                        // [B, H, Nq, d] bf16 or fp32
   const void* dout;                     // [B, H, Nq, d] bf16
   const float* lse;                     // [B, H, Nq]
-  float* dq;                            // [B, H, Nq, d] fp32 (accumulated into; zeroed by the launcher)
-  float* dk;                            // [B, H, Nk, d] fp32
-  float* dv;                            // [B, H, Nk, d] fp32
+  float* dq;                            // [B, H, Nq, d] fp32 accumulator (zeroed by the preprocess): the output
+                                        // itself for fp32 gradients, workspace for bf16 ones
+  void* dq_out;                         // [B, H, Nq, d] dQ output in the gradient type
+  void* dk;                             // [B, H, Nk, d] in the gradient type
+  void* dv;                             // [B, H, Nk, d] in the gradient type
+  int grad_bf16;                        // gradients written as bf16 (else fp32)
   uint8_t* bias;                        // workspace [B*H, n_pad / 64] blocks of 4 KB: per 64-query block the
                                         // bias tiles -LSE/scale and -rowsum(dO * O) (-inf and 0 past Nq)
   int n_pad;                            // Nq rounded up to a multiple of 64

@@ -33,7 +33,7 @@
 extern "C" {
 #endif
 
-#define FA_ABI_VERSION 1
+#define FA_ABI_VERSION 2
 
 typedef enum fa_status {
   FA_OK = 0,
@@ -93,8 +93,10 @@ fa_status fa_forward_qk(const void* q, const void* k, const void* v, void* o, fa
 
 /* Bytes of workspace fa_backward needs (pass Nq for fa_backward_qk): 64 per query row over N rounded up to a
  * multiple of 64 (per row, -LSE/scale and -rowsum(dO * O), each as three bf16
- * terms, laid out as tensor-core operand tiles). */
-size_t fa_backward_workspace_size(int B, int H, int N, int d);
+ * terms, laid out as tensor-core operand tiles); with grad_dtype FA_BF16 also
+ * the fp32 accumulator of dQ (4 * N * d bytes per (batch, head), after the
+ * tiles at a 256-byte boundary).  0 for an invalid argument. */
+size_t fa_backward_workspace_size(int B, int H, int N, int d, fa_dtype grad_dtype);
 
 /*
  * fa_backward — dQ, dK, dV of loss = sum(O * dO) by recomputing P from LSE.
@@ -106,13 +108,19 @@ size_t fa_backward_workspace_size(int B, int H, int N, int d);
  *
  *  q, k, v, dout  [B, H, N, d] bf16; o [B, H, N, d] in o_dtype (the forward's
  *                 output); lse [B, H, N] float (the forward's LSE).
- *  dq, dk, dv     [B, H, N, d] float, written (dq is zeroed and accumulated).
- *  workspace      device scratch of >= fa_backward_workspace_size() bytes.
+ *  dq, dk, dv     [B, H, N, d] in grad_dtype, written.  Every product
+ *                 accumulates in fp32; FA_BF16 rounds the final gradients to
+ *                 bf16 (dQ is accumulated in the workspace and converted by a
+ *                 second kernel), FA_F32 writes them as they are (dQ is zeroed
+ *                 and accumulated in place).  Another grad_dtype is
+ *                 FA_ERR_INVALID_ARG.
+ *  workspace      device scratch of >= fa_backward_workspace_size(..., grad_dtype) bytes.
  * The causal flag and scale must match the forward call.
  */
 fa_status fa_backward(const void* q, const void* k, const void* v, const void* o, fa_dtype o_dtype,
-                      const float* lse, const void* dout, float* dq, float* dk, float* dv, int B, int H, int N, int d,
-                      float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
+                      const float* lse, const void* dout, void* dq, void* dk, void* dv, fa_dtype grad_dtype, int B,
+                      int H, int N, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
+                      void* stream);
 
 /*
  * fa_backward_qk — fa_backward with Nq queries against Nk keys and a query offset.
@@ -123,15 +131,15 @@ fa_status fa_backward(const void* q, const void* k, const void* v, const void* o
  * get zero dK and dV.
  *
  *  q, dout, o  [B, H, Nq, d];  lse [B, H, Nq];  k, v [B, H, Nk, d].
- *  dq [B, H, Nq, d] float;  dk, dv [B, H, Nk, d] float, written.
- *  workspace   >= fa_backward_workspace_size(B, H, Nq, d) bytes.
+ *  dq [B, H, Nq, d];  dk, dv [B, H, Nk, d]; in grad_dtype, written (as for fa_backward).
+ *  workspace   >= fa_backward_workspace_size(B, H, Nq, d, grad_dtype) bytes.
  * Lengths and offset as for fa_forward_qk; they, causal and scale must match
  * the forward call.
  */
 fa_status fa_backward_qk(const void* q, const void* k, const void* v, const void* o, fa_dtype o_dtype,
-                         const float* lse, const void* dout, float* dq, float* dk, float* dv, int B, int H, int Nq,
-                         int Nk, int q_start, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
-                         void* stream);
+                         const float* lse, const void* dout, void* dq, void* dk, void* dv, fa_dtype grad_dtype, int B,
+                         int H, int Nq, int Nk, int q_start, int d, float scale, int causal, void* workspace,
+                         size_t workspace_bytes, void* stream);
 
 /* Bytes of workspace fa_decode needs: per-segment states and one arrival
  * counter per (batch, head). */

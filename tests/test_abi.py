@@ -39,15 +39,20 @@ def test_every_declared_symbol_is_exported_and_bound(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.fa_abi_version() == 1
+    assert lib.fa_abi_version() == 2
     assert lib.fa_status_string(0) == b"ok"
     assert lib.fa_status_string(4) == b"device wait timed out"
 
 
 def test_workspace_sizes(lib):
     # per query row (padded to a multiple of 64): two 32-byte rows of bias tiles
-    assert lib.fa_backward_workspace_size(2, 16, 8192, 128) == 2 * 16 * 8192 * 64
-    assert lib.fa_backward_workspace_size(1, 1, 65, 64) == 128 * 64  # rows padded to 128
+    assert lib.fa_backward_workspace_size(2, 16, 8192, 128, 1) == 2 * 16 * 8192 * 64
+    assert lib.fa_backward_workspace_size(1, 1, 65, 64, 1) == 128 * 64  # rows padded to 128
+    # bf16 gradients add the fp32 dQ accumulator after the bias tiles (256-byte aligned)
+    assert lib.fa_backward_workspace_size(2, 16, 8192, 128, 0) == 2 * 16 * 8192 * 64 + 2 * 16 * 8192 * 128 * 4
+    assert lib.fa_backward_workspace_size(1, 1, 65, 64, 0) == 8192 + 65 * 64 * 4
+    assert lib.fa_backward_workspace_size(1, 1, 3, 64, 0) == 64 * 64 + 3 * 64 * 4
+    assert lib.fa_backward_workspace_size(1, 1, 8, 64, 2) == 0
     counters = ((16 * 32 * 4 + 255) // 256) * 256
     partials = 16 * 32 * 64 * 130 * 4
     assert lib.fa_decode_workspace_size(16, 32, 128, 64) == counters + ((partials + 255) // 256) * 256
@@ -66,10 +71,15 @@ def test_forward_rejects_bad_arguments(lib):
 
 
 def test_backward_rejects_bad_arguments(lib):
+    # fa_backward(q, k, v, o, o_dtype, lse, dout, dq, dk, dv, grad_dtype, B, H, N, d, scale, causal, ws, bytes, stream)
     args = [FAKE] * 4 + [0, FAKE, FAKE, FAKE, FAKE, FAKE]
-    assert lib.fa_backward(*args, 1, 1, 8, 80, 0.0, 1, FAKE, 1 << 20, None) == 2
-    assert lib.fa_backward(*args, 1, 1, 8, 64, 0.0, 1, FAKE, 4, None) == 5
-    assert lib.fa_backward(*args, 1, 1, 8, 64, 0.0, 1, None, 1 << 20, None) == 5
+    assert lib.fa_backward(*args, 1, 1, 1, 8, 80, 0.0, 1, FAKE, 1 << 20, None) == 2
+    assert lib.fa_backward(*args, 1, 1, 1, 8, 64, 0.0, 1, FAKE, 4, None) == 5
+    assert lib.fa_backward(*args, 1, 1, 1, 8, 64, 0.0, 1, None, 1 << 20, None) == 5
+    assert lib.fa_backward(*args, 5, 1, 1, 8, 64, 0.0, 1, FAKE, 1 << 20, None) == 1  # grad_dtype
+    # bf16 gradients need the larger workspace: the fp32-gradient size is too small
+    small = lib.fa_backward_workspace_size(1, 1, 64, 64, 1)
+    assert lib.fa_backward(*args, 0, 1, 1, 64, 64, 0.0, 1, FAKE, small, None) == 5
 
 
 def test_decode_rejects_bad_arguments(lib):
@@ -88,8 +98,8 @@ def test_offset_entry_points_reject_bad_arguments(lib):
     assert lib.fa_forward_qk(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 0, 0, 64, 0.0, 1, 0, None) == 1
     assert lib.fa_forward_qk(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 16, 2**31 - 4, 64, 0.0, 1, 0, None) == 1
     assert lib.fa_forward_qk(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 16, 0, 48, 0.0, 1, 0, None) == 2
-    args = [FAKE] * 4 + [0, FAKE, FAKE, FAKE, FAKE, FAKE]
-    # fa_backward_qk(..., B, H, Nq, Nk, q_start, d, scale, causal, workspace, bytes, stream)
+    args = [FAKE] * 4 + [0, FAKE, FAKE, FAKE, FAKE, FAKE, 1]
+    # fa_backward_qk(..., grad_dtype, B, H, Nq, Nk, q_start, d, scale, causal, workspace, bytes, stream)
     assert lib.fa_backward_qk(*args, 1, 1, 8, 16, -3, 64, 0.0, 1, FAKE, 1 << 20, None) == 1
     assert lib.fa_backward_qk(*args, 1, 1, 8, 0, 0, 64, 0.0, 1, FAKE, 1 << 20, None) == 1
     assert lib.fa_backward_qk(*args, 1, 1, 8, 16, 0, 64, 0.0, 1, FAKE, 4, None) == 5
