@@ -63,10 +63,14 @@ fa_status make_grad_store_map(CUtensorMap* m, void* ptr, int BH, int N, int d, b
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+constexpr long long kMaxCount = 0x7FFFFFFFLL;
+
 fa_status check_common(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (static_cast<long long>(B) * H > 65535LL) return FA_ERR_UNSUPPORTED;  // grid.x holds B*H for fwd/bwd
+  // Heads, work items and CTAs are counted with 32-bit integers: B*H (and each
+  // launch's item or CTA count, checked where it is known) must stay below 2^31.
+  if (static_cast<long long>(B) * H > kMaxCount) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 
@@ -124,6 +128,7 @@ fa_status fa_forward_qk(const void* q, const void* k, const void* v, void* o, fa
   if (o_dtype != FA_BF16 && o_dtype != FA_F32) return FA_ERR_INVALID_ARG;
   fa_status st = check_lengths(B, H, Nq, Nk, q_start, d);
   if (st != FA_OK) return st;
+  if (static_cast<long long>(B) * H * ((Nq + 255) / 256) > kMaxCount) return FA_ERR_UNSUPPORTED;  // work items
   fa::ForwardArgs a{};
   const int BH = B * H;
   if ((st = make_row_tile_map(&a.tm_q, q, BH, Nq, d)) != FA_OK) return st;
@@ -176,6 +181,10 @@ fa_status fa_backward_qk(const void* q, const void* k, const void* v, const void
   if (grad_dtype != FA_BF16 && grad_dtype != FA_F32) return FA_ERR_INVALID_ARG;
   fa_status st = check_lengths(B, H, Nq, Nk, q_start, d);
   if (st != FA_OK) return st;
+  // one CTA per (128-key tile, head); the preprocess takes 256 / (d / 8) rows per block
+  if (static_cast<long long>(B) * H * ((Nk + 127) / 128) > kMaxCount ||
+      static_cast<long long>(B) * H * ((Nq + 63) / 64 * 64) / (256 / (d / 8)) > kMaxCount)
+    return FA_ERR_UNSUPPORTED;
   if (!workspace || !aligned16(workspace) || workspace_bytes < fa_backward_workspace_size(B, H, Nq, d, grad_dtype))
     return FA_ERR_WORKSPACE;
   const bool grad_bf16 = grad_dtype == FA_BF16;

@@ -22,7 +22,9 @@
  *    launch returns FA_ERR_CUDA.  A kernel that hits its internal wait limit
  *    (it never hangs) records FA_ERR_TIMEOUT, read by fa_device_status().
  *  - Supported: d in {64, 128}; N >= 1 (any N: ragged last tiles are masked);
- *    B * H <= 65535 * 65535.
+ *    B * H < 2^31, and the forward's B * H * ceil(Nq / 256) work items and the
+ *    backward's B * H * ceil(Nk / 128) CTAs below 2^31 as well
+ *    (FA_ERR_UNSUPPORTED otherwise); fa_decode: B, H <= 65535.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H

@@ -105,6 +105,15 @@ def test_offset_entry_points_reject_bad_arguments(lib):
     assert lib.fa_backward_qk(*args, 1, 1, 8, 16, 0, 64, 0.0, 1, FAKE, 4, None) == 5
 
 
+def test_counts_beyond_32_bits_are_unsupported(lib):
+    # B * H = 2^31 heads; then 2^30 heads whose forward items (ceil(1024 / 256) each)
+    # or backward CTAs (ceil(1024 / 128) each) pass 2^31: rejected before any CUDA call
+    assert lib.fa_forward(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1 << 16, 1 << 15, 8, 64, 0.0, 0, 0, None) == 2
+    assert lib.fa_forward(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1 << 20, 1 << 10, 1024, 64, 0.0, 0, 0, None) == 2
+    args = [FAKE] * 4 + [0, FAKE, FAKE, FAKE, FAKE, FAKE, 1]
+    assert lib.fa_backward(*args, 1 << 20, 1 << 10, 1024, 64, 0.0, 0, FAKE, 1 << 62, None) == 2
+
+
 def test_merge_and_auto_split_reject_bad_arguments(lib):
     # fa_merge_states(o_a, lse_a, o_b, lse_b, o, lse, o_dtype, rows, d, stream)
     assert lib.fa_merge_states(None, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 128, None) == 1

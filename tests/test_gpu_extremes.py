@@ -1,7 +1,8 @@
 """Parity at the extremes of the sizes the kernels take: a long ragged sequence
 (the forward's grid along N and its last, partial query tile), thousands of heads
-with a single ragged key tile each (the backward's grid along batch*head), and a
-long ragged decode context.  Same bars as the other parity tests."""
+with a single ragged key tile each (the backward's grid along batch*head), more
+heads than a grid's y or z dimension holds, and a long ragged decode context.
+Same bars as the other parity tests."""
 import numpy as np
 import pytest
 import torch
@@ -58,6 +59,33 @@ def test_backward_4096_heads_of_one_ragged_tile(causal):
         for name, got, r in zip(("dQ", "dK", "dV"), (dq[b, h], dk[b, h], dv[b, h]), ref):
             err = rel_fro(f64(got), r)
             assert err <= GRAD_REL_FRO, f"{name} of ({b}, {h}): relative Frobenius error {err:.3e}"
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_more_heads_than_a_grid_dimension(causal):
+    """B=70, H=1000: 70 000 heads (more than 65535, the limit of a grid's y and z
+    dimensions) of N=20, d=64, forward and backward.  Heads on both sides of 65535
+    against the oracle, every output finite."""
+    from exact_attention_flash_gb300 import fa_backward, fa_device_status, fa_forward
+    from exact_attention_flash_gb300.workloads import make_attention_inputs
+    from oracle import attention_dense
+
+    q, k, v, do = make_attention_inputs(70, 1000, 20, 64, 14, "cuda")
+    o, lse = fa_forward(q, k, v, causal=causal)
+    dq, dk, dv = fa_backward(q, k, v, o, lse, do, causal=causal, grad_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert fa_device_status() == 0
+    for t in (o, lse, dq, dk, dv):
+        assert torch.isfinite(t).all()
+    for flat in (0, 4321, 65534, 65535, 65536, 69999):
+        b, h = divmod(flat, 1000)
+        ref_o, ref_l = attention_dense(f64(q[b, h]), f64(k[b, h]), f64(v[b, h]), causal=causal)
+        assert o_within_bar(f64(o[b, h]), ref_o, "bf16") <= 0.0
+        assert max_abs(f64(lse[b, h]), ref_l) <= LSE_MAX_ABS
+        ref = attention_dense_backward(f64(q[b, h]), f64(k[b, h]), f64(v[b, h]), f64(do[b, h]), causal=causal)
+        for name, got, r in zip(("dQ", "dK", "dV"), (dq[b, h], dk[b, h], dv[b, h]), ref):
+            err = rel_fro(f64(got), r)
+            assert err <= GRAD_REL_FRO, f"{name} of head {flat}: relative Frobenius error {err:.3e}"
 
 
 def test_decode_long_ragged_context():
