@@ -40,8 +40,11 @@ namespace {
 __device__ unsigned g_fwd_status;
 // Scheduling slots of the persistent forward: {items claimed, CTAs finished}.  Each
 // launch takes the next slot in turn, so launches that overlap on different
-// streams count on different slots; each launch leaves its slot at zero.
-constexpr int kSchedSlots = 64;
+// streams count on different slots; each launch leaves its slot at zero.  Two
+// launches share a slot only if they are kSchedSlots apart in issue order and
+// still run at the same time (a launch captured in a CUDA graph keeps its slot for
+// every replay; replays of one graph run one after another).
+constexpr int kSchedSlots = 4096;
 __device__ unsigned g_fwd_sched[kSchedSlots][2];
 
 constexpr int kBM = 128;             // query rows per tile (TMEM lanes)
