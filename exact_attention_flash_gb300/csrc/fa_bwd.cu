@@ -5,10 +5,10 @@
 // ``flash_backward``; "lab.py" ``backward``): D = rowsum(dO * O); for each key
 // tile j and query tile i, S = Q_i K_j^T * scale, P = exp(S - L_i),
 // dV_j += P^T dO_i, dP = dO_i V_j^T, dS = P * (dP - D_i),
-// dQ_i += dS K_j * scale, dK_j += dS^T Q_i * scale.  Causal (query i at position
-// q_start + i sees key j iff j <= q_start + i): query tiles that lie wholly before
-// the key tile are skipped, the others are masked per element, and a key tile that
-// no query sees gets zero dK and dV.
+// dQ_i += dS K_j * scale, dK_j += dS^T Q_i * scale (the scale is folded into dS).
+// Causal (query i at position q_start + i sees key j iff j <= q_start + i): query
+// tiles that lie wholly before the key tile are skipped, the others are masked per
+// element, and a key tile that no query sees gets zero dK and dV.
 //
 // Kernels:
 //   bwd_preprocess  D/8 lanes per row: D = rowsum(dO * O), the per-query biases
@@ -423,14 +423,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         break;
       }
       tc_fence_after();
-      // dS^T = P^T * (dP^T - D); dP^T arrives holding dP^T - D.
+      // dS^T = P^T * (dP^T - D); dP^T arrives holding dP^T - D.  The softmax scale of
+      // dQ = dS K * scale and dK = dS^T Q * scale is applied here, once per element of
+      // dS (rounding scale * dS to bf16 has the relative error of rounding dS), so the
+      // dQ writers and the dK epilogue add and store the products as they are.
       uint32_t dpv[32];
       tmem_ld32(dp_tm, dpv);
       uint32_t dk[16];
+      const float2 sc2 = make_float2(a.scale, a.scale);
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
-        const float2 ds2 =
-            __fmul2_rn(make_float2(p[e], p[e + 1]), make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])));
+        const float2 ds2 = __fmul2_rn(__fmul2_rn(make_float2(p[e], p[e + 1]), sc2),
+                                      make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])));
         dk[e / 2] = pack_bf16(ds2.x, ds2.y);
       }
       // dS^T row of this key into the MN-major, 128B-swizzled dS tile:
@@ -473,25 +477,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
           for (int j = 0; j < 4; ++j) {
             const uint32_t* w = uv + 8 * j;
             const uint32_t* x = uk + 8 * j;
-            const float s = a.scale;
             *reinterpret_cast<uint4*>(rv + (((j0 + j) ^ (k & 7)) << 4)) =
                 make_uint4(pack_bf16(__uint_as_float(w[0]), __uint_as_float(w[1])),
                            pack_bf16(__uint_as_float(w[2]), __uint_as_float(w[3])),
                            pack_bf16(__uint_as_float(w[4]), __uint_as_float(w[5])),
                            pack_bf16(__uint_as_float(w[6]), __uint_as_float(w[7])));
             *reinterpret_cast<uint4*>(rk + (((j0 + j) ^ (k & 7)) << 4)) =
-                make_uint4(pack_bf16(__uint_as_float(x[0]) * s, __uint_as_float(x[1]) * s),
-                           pack_bf16(__uint_as_float(x[2]) * s, __uint_as_float(x[3]) * s),
-                           pack_bf16(__uint_as_float(x[4]) * s, __uint_as_float(x[5]) * s),
-                           pack_bf16(__uint_as_float(x[6]) * s, __uint_as_float(x[7]) * s));
+                make_uint4(pack_bf16(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                           pack_bf16(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                           pack_bf16(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                           pack_bf16(__uint_as_float(x[6]), __uint_as_float(x[7])));
           }
         } else {
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             *reinterpret_cast<uint4*>(rv + ((j ^ (k & 7)) << 4)) = make_uint4(uv[4 * j], uv[4 * j + 1], uv[4 * j + 2], uv[4 * j + 3]);
-            *reinterpret_cast<float4*>(rk + ((j ^ (k & 7)) << 4)) =
-                make_float4(__uint_as_float(uk[4 * j]) * a.scale, __uint_as_float(uk[4 * j + 1]) * a.scale,
-                            __uint_as_float(uk[4 * j + 2]) * a.scale, __uint_as_float(uk[4 * j + 3]) * a.scale);
+            *reinterpret_cast<uint4*>(rk + ((j ^ (k & 7)) << 4)) = make_uint4(uk[4 * j], uk[4 * j + 1], uk[4 * j + 2], uk[4 * j + 3]);
           }
         }
       }
@@ -538,8 +539,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         const int rows = min(32, a.Nq - q0);
 #pragma unroll
         for (int kq = 0; kq < 8; ++kq) {
-          const float x0 = __uint_as_float(v[4 * kq]) * a.scale, x1 = __uint_as_float(v[4 * kq + 1]) * a.scale;
-          const float x2 = __uint_as_float(v[4 * kq + 2]) * a.scale, x3 = __uint_as_float(v[4 * kq + 3]) * a.scale;
+          const float x0 = __uint_as_float(v[4 * kq]), x1 = __uint_as_float(v[4 * kq + 1]);
+          const float x2 = __uint_as_float(v[4 * kq + 2]), x3 = __uint_as_float(v[4 * kq + 3]);
           // Exchange 1 (lanes i, i ^ 1): even lanes keep queries 0 and 2, odd lanes 1 and 3,
           // each for both features of the pair.
           const bool odd = i4 & 1;
