@@ -8,7 +8,12 @@ from __future__ import annotations
 import ctypes
 from pathlib import Path
 
-LIB_PATH = Path(__file__).resolve().parent / "libfa_gb300.so"
+import os
+
+# The library to load: the in-tree build, or another build of the same sources named
+# by FA_GB300_LIBRARY (the bounds-checked one, libfa_gb300_checked.so).
+LIB_PATH = Path(os.environ["FA_GB300_LIBRARY"]) if os.environ.get("FA_GB300_LIBRARY") else (
+    Path(__file__).resolve().parent / "libfa_gb300.so")
 
 FA_OK = 0
 STATUS_NAMES = {
@@ -18,6 +23,7 @@ STATUS_NAMES = {
     3: "FA_ERR_CUDA",
     4: "FA_ERR_TIMEOUT",
     5: "FA_ERR_WORKSPACE",
+    6: "FA_ERR_BOUNDS",
 }
 FA_BF16 = 0
 FA_F32 = 1

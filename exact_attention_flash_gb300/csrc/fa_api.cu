@@ -111,6 +111,7 @@ const char* fa_status_string(fa_status s) {
     case FA_ERR_CUDA: return "CUDA error";
     case FA_ERR_TIMEOUT: return "device wait timed out";
     case FA_ERR_WORKSPACE: return "workspace missing or too small";
+    case FA_ERR_BOUNDS: return "index outside its buffer (bounds-checked build)";
   }
   return "unknown status";
 }
@@ -304,12 +305,14 @@ fa_status fa_forward_keymajor(const void* q, const void* k, const void* v, void*
 
 fa_status fa_device_status(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  unsigned f = 0, b = 0, dcd = 0, km = 0;
+  unsigned f = 0, b = 0, dcd = 0, km = 0, mg = 0;
   if (fa::read_clear_forward_status(&f, s) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::read_clear_backward_status(&b, s) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::read_clear_decode_status(&dcd, s) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::read_clear_keymajor_status(&km, s) != cudaSuccess) return FA_ERR_CUDA;
-  const unsigned all = f | b | dcd | km;
+  if (fa::read_clear_merge_status(&mg, s) != cudaSuccess) return FA_ERR_CUDA;
+  const unsigned all = f | b | dcd | km | mg;
+  if (all & 4u) return FA_ERR_BOUNDS;  // only the bounds-checked build sets it
   if (all & 1u) return FA_ERR_TIMEOUT;
   if (all != 0u) return FA_ERR_CUDA;
   return FA_OK;

@@ -160,6 +160,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     const size_t off = (static_cast<size_t>(bh) * a.Nk + key0) * row_bytes;
     uint4* dk4 = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.dk) + off);
     uint4* dv4 = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.dv) + off);
+    // the tile's rows of dK and dV, in 16-byte pieces of [B, H, Nk, D]
+    const long long pieces = static_cast<long long>(a.B) * a.H * a.Nk * row_bytes / 16;
+    if (!in_bounds(static_cast<long long>(off / 16) + rows * row_bytes / 16 - 1, pieces, &g_bwd_status)) return;
     for (int i = tid; i < rows * row_bytes / 16; i += kBwdThreads) {
       dk4[i] = make_uint4(0u, 0u, 0u, 0u);
       dv4[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -221,14 +224,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
           if (n >= C::kStages && !mbar_wait(&sh.q_empty[s], ((n / C::kStages) - 1) & 1, &sh.abort, &g_bwd_status))
             break;
           const int q0 = (i_start + n) * kBQ;
-          mbar_arrive_expect_tx(&sh.q_full[s], 2 * C::kQBytes + C::kBiasBytes);
+          // The query block's bias tiles from the workspace (4 KB aligned): block blk of
+          // the B * H * n_pad / 64 blocks.
+          const size_t blk = static_cast<size_t>(bh) * (a.n_pad / kBQ) + (i_start + n);
+          const bool bias_ok = in_bounds(static_cast<long long>(blk), static_cast<long long>(a.B) * a.H * (a.n_pad / kBQ),
+                                         &g_bwd_status);
+          mbar_arrive_expect_tx(&sh.q_full[s], 2 * C::kQBytes + (bias_ok ? C::kBiasBytes : 0));
           for (int c = 0; c < D / 64; ++c) {
             tma_load_3d(sQ + s * C::kQBytes + c * (kBQ * 128), &a.tm_q, &sh.q_full[s], c * 64, q0, bh);
             tma_load_3d(sDO + s * C::kQBytes + c * (kBQ * 128), &a.tm_do, &sh.q_full[s], c * 64, q0, bh);
           }
-          // The query block's bias tiles from the workspace (always in bounds, 4 KB aligned).
-          const size_t blk = static_cast<size_t>(bh) * (a.n_pad / kBQ) + (i_start + n);
-          bulk_load(sBias + s * C::kBiasBytes, a.bias + blk * C::kBiasBytes, C::kBiasBytes, &sh.q_full[s]);
+          if (bias_ok) bulk_load(sBias + s * C::kBiasBytes, a.bias + blk * C::kBiasBytes, C::kBiasBytes, &sh.q_full[s]);
           ++issued;
         }
         mbar_wait_drain(&sh.kv_full, 0);
@@ -535,8 +541,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         // instruction then covers four whole 128-byte row segments, a quarter of the
         // instructions of one reduction per feature.
         const int i4 = lane & 3;
-        float* dst = a.dq + (static_cast<size_t>(bh) * a.Nq + q0 + i4) * D + lane_base + 4 * (lane >> 2);
+        const long long dst_idx = (static_cast<long long>(bh) * a.Nq + q0 + i4) * D + lane_base + 4 * (lane >> 2);
+        float* dst = a.dq + dst_idx;
         const int rows = min(32, a.Nq - q0);
+        const long long dq_elems = static_cast<long long>(a.B) * a.H * a.Nq * D;
 #pragma unroll
         for (int kq = 0; kq < 8; ++kq) {
           const float x0 = __uint_as_float(v[4 * kq]), x1 = __uint_as_float(v[4 * kq + 1]);
@@ -552,7 +560,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
           const float t0 = __shfl_xor_sync(0xffffffffu, hi ? a0 : a2, 2);
           const float t1 = __shfl_xor_sync(0xffffffffu, hi ? a1 : a3, 2);
           const float y0 = hi ? t0 : a0, y1 = hi ? t1 : a1, y2 = hi ? a2 : t0, y3 = hi ? a3 : t1;
-          if (4 * kq + i4 < rows) {
+          if (4 * kq + i4 < rows && in_bounds(dst_idx + 4LL * kq * D + 3, dq_elems, &g_bwd_status)) {
             asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + static_cast<size_t>(4 * kq) * D),
                          "f"(y0), "f"(y1), "f"(y2), "f"(y3)
                          : "memory");
@@ -608,8 +616,10 @@ __global__ void __launch_bounds__(256) bwd_preprocess(const void* __restrict__ o
   const bool live = prow < padded_rows;
   const long long bh = live ? prow / n_pad : 0;
   const int q = live ? static_cast<int>(prow - bh * n_pad) : 0;
+  const long long n_bh = padded_rows / n_pad;  // B * H
   float acc = 0.f;
-  if (live && q < N) {
+  if (live && q < N &&
+      in_bounds((bh * N + q) * D + sub * 8 + 7, n_bh * N * D, &g_bwd_status)) {  // dO, O and dQ [B, H, N, D]
     const size_t base = static_cast<size_t>(bh * N + q) * D + sub * 8;
     const uint4 dv = *reinterpret_cast<const uint4*>(dout + base);
     float ov[8];
@@ -640,12 +650,16 @@ __global__ void __launch_bounds__(256) bwd_preprocess(const void* __restrict__ o
 #pragma unroll
   for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (live && sub < 4) {  // sub: tile (sub >> 1: 0 = LSE, 1 = D), piece (sub & 1)
-    const float bs = q < N ? -lse[bh * N + q] * inv_scale : -INFINITY;
+    const bool lse_ok = q < N && in_bounds(bh * N + q, n_bh * N, &g_bwd_status);
+    const float bs = lse_ok ? -lse[bh * N + q] * inv_scale : -INFINITY;
     const float bd = q < N ? -acc : 0.f;
     const int r = q & (kBQ - 1);
-    uint8_t* tile = bias + (static_cast<size_t>(bh) * (n_pad / kBQ) + q / kBQ) * (2 * kBQ * 32) + (sub >> 1) * (kBQ * 32);
+    const size_t tile_off = (static_cast<size_t>(bh) * (n_pad / kBQ) + q / kBQ) * (2 * kBQ * 32) + (sub >> 1) * (kBQ * 32);
     const int off = ((r >> 3) * 2 + (sub & 1)) * 128 + (r & 7) * 16;
-    *reinterpret_cast<uint4*>(tile + off) = (sub & 1) ? make_uint4(0u, 0u, 0u, 0u) : bias_terms((sub >> 1) ? bd : bs);
+    // 16-byte pieces of the B * H * n_pad * 64-byte workspace
+    if (in_bounds(static_cast<long long>((tile_off + off) / 16), padded_rows * 4, &g_bwd_status))
+      *reinterpret_cast<uint4*>(bias + tile_off + off) =
+          (sub & 1) ? make_uint4(0u, 0u, 0u, 0u) : bias_terms((sub >> 1) ? bd : bs);
   }
 }
 

@@ -91,8 +91,14 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_split_kernel(DecodeArgs
   const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(a.k) + static_cast<size_t>(bh) * a.L * D;
   const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(a.v) + static_cast<size_t>(bh) * a.L * D;
 
+  // Logical extents for the bounds-checked build: q and o [B*H, D], k and v
+  // [B*H, L, D], the segment states [B*H, n_split, D + 2], the counters [B*H].
+  const long long n_bh = static_cast<long long>(a.B) * a.H;
   float qf[8];
-  bf16x8_to_float(*reinterpret_cast<const uint4*>(qp + sub * 8), qf);
+  bf16x8_to_float(in_bounds(static_cast<long long>(bh) * D + sub * 8 + 7, n_bh * D, &g_decode_status)
+                      ? *reinterpret_cast<const uint4*>(qp + sub * 8)
+                      : make_uint4(0u, 0u, 0u, 0u),
+                  qf);
 #pragma unroll
   for (int i = 0; i < 8; ++i) qf[i] *= a.scale_log2;
 
@@ -107,7 +113,8 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_split_kernel(DecodeArgs
 #pragma unroll
     for (int u = 0; u < kDecodeUnroll; ++u) {
       const int key = base0 + u * kGroups + group;
-      if (key < j1) {
+      if (key < j1 && in_bounds((static_cast<long long>(bh) * a.L + key) * D + sub * 8 + 7, n_bh * a.L * D,
+                                &g_decode_status)) {
         kr[u] = __ldcs(reinterpret_cast<const uint4*>(kp + static_cast<size_t>(key) * D + sub * 8));
         vr[u] = __ldcs(reinterpret_cast<const uint4*>(vp + static_cast<size_t>(key) * D + sub * 8));
       } else {
@@ -159,7 +166,9 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_split_kernel(DecodeArgs
   __syncthreads();
 
   float* ws = a.ws_partials + (static_cast<size_t>(bh) * a.n_split + split) * kStateStride;
-  if (tid < D) {
+  const long long n_states = n_bh * a.n_split;
+  if (tid < D && in_bounds((static_cast<long long>(bh) * a.n_split + split + 1) * kStateStride - 1,
+                           n_states * kStateStride, &g_decode_status)) {
     float pm = -INFINITY, pl = 0.f, po = 0.f;
     for (int g = 0; g < kGroups; ++g) merge_into(pm, pl, &po, sh_m[g], sh_l[g], &sh_o[g][tid], 1);
     ws[2 + tid] = po;
@@ -183,14 +192,19 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_split_kernel(DecodeArgs
   __threadfence();
   __syncthreads();
   if (tid == 0) {
-    const unsigned prev = atomicAdd(&a.ws_counters[bh], 1u);
-    sh_last = (prev == static_cast<unsigned>(a.n_split - 1)) ? 1 : 0;
+    if (in_bounds(bh, n_bh, &g_decode_status)) {
+      const unsigned prev = atomicAdd(&a.ws_counters[bh], 1u);
+      sh_last = (prev == static_cast<unsigned>(a.n_split - 1)) ? 1 : 0;
+    } else {
+      sh_last = 0;
+    }
   }
   __syncthreads();
   if (!sh_last) return;
   __threadfence();
 
-  if (tid < D) {
+  if (tid < D && in_bounds((static_cast<long long>(bh) + 1) * a.n_split * kStateStride - 1, n_states * kStateStride,
+                           &g_decode_status)) {
     const float* base = a.ws_partials + static_cast<size_t>(bh) * a.n_split * kStateStride;
     float fm = -INFINITY, fl = 0.f, fo = 0.f;
     for (int s = 0; s < a.n_split; ++s) {

@@ -518,10 +518,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     {
       const float inv_l = 1.f / l_hat;
       const size_t row_off = (static_cast<size_t>(bh) * a.Nq + row) * D;
+      const long long rows_total = static_cast<long long>(a.B) * a.H * a.Nq;
+      // the row's D elements of O and its LSE lie inside [B, H, Nq, D] and [B, H, Nq]
+      const bool store = row < a.Nq && in_bounds(static_cast<long long>(row_off) + D - 1, rows_total * D, &g_fwd_status) &&
+                         in_bounds(static_cast<long long>(bh) * a.Nq + row, rows_total, &g_fwd_status);
 #pragma unroll
       for (int c = 0; c < D; c += 32) {
         const uint32_t* u = orow + c;
-        if (row < a.Nq) {
+        if (store) {
           if (a.o_f32) {
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.o) + row_off + c);
 #pragma unroll
@@ -541,7 +545,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           }
         }
       }
-      if (row < a.Nq) a.lse[static_cast<size_t>(bh) * a.Nq + row] = (m_run + __log2f(l_run)) * kLn2;
+      if (store) a.lse[static_cast<size_t>(bh) * a.Nq + row] = (m_run + __log2f(l_run)) * kLn2;
     }
     }
     if (a.stats != nullptr) {  // fa_set_stats counters: one addition per warp and CTA

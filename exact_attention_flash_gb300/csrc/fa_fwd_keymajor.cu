@@ -205,7 +205,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa1_kernel(const __grid_constant_
         for (int c = 0; c < D; c += 64) tmem_ld64(pv_tm + c, *reinterpret_cast<uint32_t (*)[64]>(pv + c));
         tc_fence_before();
         mbar_arrive_warp(&sh.done);  // S and p~ V may be overwritten by the next pair
-        if (row < a.N) {
+        // the row's state in the [B*H, N] and [B*H, N, D] workspace arrays
+        if (row < a.N && in_bounds(static_cast<long long>(bh) * a.N + row, static_cast<long long>(a.B) * a.H * a.N,
+                                   &g_fa1_status)) {
           const size_t rix = static_cast<size_t>(bh) * a.N + row;
           float* orow = a.ws_o + rix * D;
           // The row's state before this visit (key tile 0 is every row's first visit).
@@ -236,7 +238,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa1_kernel(const __grid_constant_
     if (ok) {
       for (int i = 0; i < n_t; ++i) {
         const int row = i * kT + r;
-        if (row >= a.N) continue;
+        if (row >= a.N ||
+            !in_bounds(static_cast<long long>(bh) * a.N + row, static_cast<long long>(a.B) * a.H * a.N, &g_fa1_status))
+          continue;
         const size_t rix = static_cast<size_t>(bh) * a.N + row;
         const float* orow = a.ws_o + rix * D;
         for (int c = 0; c < D; c += 8) {

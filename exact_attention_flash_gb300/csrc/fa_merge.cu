@@ -21,9 +21,12 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace fa {
 namespace {
+
+__device__ unsigned g_merge_status;
 
 struct Vec4 {
   float x[4];
@@ -71,6 +74,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const void* __restrict__ o_a
     const float ca = wa * inv, cb = wb * inv;
     const long long base = row * d;
     for (int e = 4 * lane; e < d; e += 128) {
+      if (!in_bounds(base + e + 3, rows * d, &g_merge_status)) continue;  // O rows [rows, d]
       const Vec4 va = load4(o_a, base + e, f32), vb = load4(o_b, base + e, f32);
       Vec4 r;
 #pragma unroll
@@ -96,6 +100,17 @@ cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b, c
   const unsigned grid = static_cast<unsigned>(blocks_needed < cap ? blocks_needed : cap);
   merge_kernel<<<grid, 256, 0, stream>>>(o_a, lse_a, o_b, lse_b, o, lse, rows, d, o_f32);
   return cudaGetLastError();
+}
+
+cudaError_t read_clear_merge_status(unsigned* out, cudaStream_t stream) {
+  cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_merge_status, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return e;
+  const unsigned zero = 0;
+  e = cudaMemcpyToSymbolAsync(g_merge_status, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(stream);
 }
 
 int decode_auto_split(int BH, int L, int sms) {

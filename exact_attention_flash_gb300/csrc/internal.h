@@ -99,6 +99,7 @@ cudaError_t launch_forward_keymajor(const KeyMajorArgs& a, cudaStream_t stream);
 
 // Merge of two (O, LSE) results over disjoint key sets (fa_merge.cu); o_f32: O is
 // fp32, else bf16.  O rows of d elements, d a multiple of 4.
+cudaError_t read_clear_merge_status(unsigned* out, cudaStream_t stream);
 cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o, float* lse,
                          long long rows, int d, int o_f32, cudaStream_t stream);
 

@@ -17,6 +17,23 @@ namespace fa {
 // Device status bits (OR-ed into a per-translation-unit status word).
 constexpr unsigned kDevTimeout = 1u;     // an mbarrier wait exceeded its limit
 constexpr unsigned kDevBadConfig = 2u;   // a kernel saw a launch shape it does not handle
+constexpr unsigned kDevBounds = 4u;      // the bounds-checked build caught an index outside its buffer
+
+// Index check of the bounds-checked build (compiled with FA_BOUNDS_CHECK).  That build
+// checks every computed (non-TMA) global access against the logical extent of its
+// buffer, as elements [0, n): an index outside sets kDevBounds in the kernel's status
+// word and the access is skipped.  In the normal build the check is constant true and
+// compiles away.  TMA tile accesses need none: the hardware drops or zero-fills rows
+// outside the tensor map.
+#ifdef FA_BOUNDS_CHECK
+__device__ __forceinline__ bool in_bounds(long long i, long long n, unsigned* status) {
+  if (i >= 0 && i < n) return true;
+  atomicOr(status, kDevBounds);
+  return false;
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(long long, long long, unsigned*) { return true; }
+#endif
 
 // Wall-clock limit for one wait.  Every wait in these kernels is on work that
 // the same CTA issued a few microseconds earlier; one second means it is broken.

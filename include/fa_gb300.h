@@ -43,7 +43,9 @@ typedef enum fa_status {
   FA_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. d not in {64, 128}) */
   FA_ERR_CUDA = 3,        /* a CUDA call or launch failed */
   FA_ERR_TIMEOUT = 4,     /* a kernel gave up waiting (reported by fa_device_status) */
-  FA_ERR_WORKSPACE = 5    /* workspace missing or smaller than the *_workspace_size() */
+  FA_ERR_WORKSPACE = 5,   /* workspace missing or smaller than the *_workspace_size() */
+  FA_ERR_BOUNDS = 6       /* a kernel of the bounds-checked build (FA_BOUNDS_CHECK) caught an index
+                             outside its buffer and skipped the access (reported by fa_device_status) */
 } fa_status;
 
 typedef enum fa_dtype { FA_BF16 = 0, FA_F32 = 1 } fa_dtype;
