@@ -7,6 +7,7 @@ kernels of ``libfa_gb300.so`` reached through its C ABI (``include/fa_gb300.h``)
 from __future__ import annotations
 
 import contextlib
+import functools
 
 import torch
 
@@ -19,6 +20,21 @@ __all__ = ["fa_forward", "fa_backward", "fa_decode", "fa_device_status", "FAErro
 
 # Order of the counters behind fa_set_stats ("attention_kernels.py" sections 3-4, ``stats``).
 STATS_FIELDS = ("tiles", "skipped", "rescales", "dq_atomic_adds")
+
+
+def _on_tensor_device(fn):
+    """Make the first argument's GPU the current device for the call, so that the
+    library launches there and on that device's current stream."""
+    @functools.wraps(fn)
+    def wrapper(t, *args, **kwargs):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda):
+            return fn(t, *args, **kwargs)  # the argument checks raise
+        others = [a for a in list(args) + list(kwargs.values()) if isinstance(a, torch.Tensor)]
+        if any(a.device != t.device for a in others):
+            raise ValueError(f"{fn.__name__}: every tensor must be on {t.device}")
+        with torch.cuda.device(t.device):
+            return fn(t, *args, **kwargs)
+    return wrapper
 
 
 def _stream_ptr(stream) -> int:
@@ -42,6 +58,7 @@ def _check_out(name, t, shape, dtypes):
         raise ValueError(f"{name} must be a contiguous CUDA tensor of shape {tuple(shape)} and dtype in {dtypes}")
 
 
+@_on_tensor_device
 def fa_forward(q, k, v, causal=False, scale=None, out_dtype=torch.bfloat16, precise=False, out=None, lse=None,
                stream=None, q_start=0):
     """O, LSE = softmax(Q K^T * scale [causal]) V.
@@ -85,6 +102,7 @@ def _grad_code(grad_dtype):
     raise ValueError("grad_dtype must be torch.float32 or torch.bfloat16")
 
 
+@_on_tensor_device
 def fa_backward(q, k, v, o, lse, do, causal=False, scale=None, workspace=None, dq=None, dk=None, dv=None,
                 stream=None, q_start=0, grad_dtype=torch.float32):
     """dQ, dK, dV of sum(O * dO) by recomputation from LSE.
@@ -136,6 +154,7 @@ def decode_auto_split(B, H, L) -> int:
     return n
 
 
+@_on_tensor_device
 def fa_decode(q, k, v, n_split=None, scale=None, return_partials=False, workspace=None, out=None, lse=None,
               stream=None):
     """Split-KV decode: q [B, H, 1, d], k/v [B, H, L, d] bf16 -> O [B, H, 1, d] fp32, LSE [B, H].
@@ -200,6 +219,7 @@ def stats_counters(device=None):
         fa_set_stats(None)
 
 
+@_on_tensor_device
 def fa_merge_states(o_a, lse_a, o_b, lse_b, out=None, lse=None, stream=None):
     """Merge two attention results over disjoint key sets ("attention_kernels.py" section 1 ``merge_states``).
 
@@ -227,6 +247,7 @@ def fa_merge_states(o_a, lse_a, o_b, lse_b, out=None, lse=None, stream=None):
     return out, lse
 
 
+@_on_tensor_device
 def fa_forward_keymajor(q, k, v, causal=False, scale=None, out_dtype=torch.bfloat16, workspace=None, stream=None):
     """O, LSE as :func:`fa_forward` gives them, computed in the first algorithm's key-major loop order.
 
