@@ -1,4 +1,5 @@
-"""bench.py --oracle-configs on CPU: the oracle's per-workload wall-clock report.
+"""bench.py's CPU legs: --oracle-configs (the oracle's per-workload wall-clock report) and the
+reference arm's JSON line.
 
 Tiny stand-ins for the named workloads keep this fast. The test checks:
 - one JSON line per workload;
@@ -56,3 +57,29 @@ def test_rowwise_extrapolation_matches_pair_counts(causal, N):
     else:
         exact = (N * N) / (rows * N)
     assert abs(factor / exact - 1.0) <= 2e-3
+
+
+def test_reference_arm_line_follows_the_contract(monkeypatch, capsys):
+    """bench.py --impl reference times the oracle and prints one JSON line with the
+    contract's keys. The line has impl = reference, the GPU arm's metric, unit and
+    direction, a cpu_baseline describing the run, and an e2e object with zero copy
+    bytes. Tiny stand-ins of the bench's two workloads keep it fast."""
+    import bench
+    from exact_attention_flash_gb300 import workloads as wl
+
+    tiny = dict(wl.WORKLOADS)
+    tiny[bench.FWD_BWD] = wl.Workload(bench.FWD_BWD, "attention", 1, 2, 96, 64, seed=2, causal=True, backward=True,
+                                      qk_mult=8.0)
+    tiny[bench.DECODE] = wl.Workload(bench.DECODE, "decode", 1, 8, 300, 64, seed=4, n_split=4)
+    monkeypatch.setattr(wl, "WORKLOADS", tiny)
+    args = type("A", (), {"steps": 2, "warmup": 1, "impl": "reference"})()
+    bench.run_reference(args, 1, 0)
+    lines = [json.loads(x) for x in capsys.readouterr().out.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    r = lines[0]
+    assert r["impl"] == "reference" and r["metric"] == bench.METRIC and r["unit"] == "TFLOP/s"
+    assert r["higher_is_better"] is True and r["steps"] == 2 and r["warmup"] == 1 and r["n_gpus"] == 1
+    assert r["value"] > 0 and r["dtype"] == "f64" and r["config"]["workload"] == bench.FWD_BWD
+    assert r["cpu_baseline"]["kind"] == "oracle" and r["cpu_baseline"]["value"] == r["value"]
+    assert r["cpu_baseline"]["cores"] >= 1 and r["cpu_baseline"]["sample"]
+    assert r["e2e"] == {"value": r["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
