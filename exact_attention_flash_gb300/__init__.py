@@ -14,7 +14,8 @@ import torch
 from . import _lib
 from ._lib import FAError
 
-__all__ = ["fa_forward", "fa_backward", "fa_decode", "fa_device_status", "FAError", "backward_workspace_bytes",
+__all__ = ["flash_attention", "fa_forward", "fa_backward", "fa_decode", "fa_device_status", "FAError",
+           "backward_workspace_bytes",
            "decode_workspace_bytes", "fa_set_stats", "stats_counters", "STATS_FIELDS", "fa_merge_states",
            "decode_auto_split", "fa_forward_keymajor"]
 
@@ -270,3 +271,36 @@ def fa_forward_keymajor(q, k, v, causal=False, scale=None, out_dtype=torch.bfloa
                                    workspace.numel(), _stream_ptr(stream))
     _lib.check("fa_forward_keymajor", code)
     return out, lse
+
+
+class _FlashAttention(torch.autograd.Function):
+    """fa_forward as the forward of an autograd node and fa_backward as its backward.
+
+    The node saves Q, K, V, O and LSE. Its backward recomputes P from LSE, as the
+    page's backward does. Autograd wants gradients in the inputs' dtype, so the
+    gradients come back as bf16; every product still accumulates in fp32.
+    """
+
+    @staticmethod
+    def forward(ctx, q, k, v, causal, scale, q_start):
+        o, lse = fa_forward(q, k, v, causal=causal, scale=scale, q_start=q_start)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.causal, ctx.scale, ctx.q_start = causal, scale, q_start
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv = fa_backward(q, k, v, o, lse, do.to(torch.bfloat16).contiguous(), causal=ctx.causal,
+                                 scale=ctx.scale, q_start=ctx.q_start, grad_dtype=torch.bfloat16)
+        return dq, dk, dv, None, None, None
+
+
+def flash_attention(q, k, v, causal=False, scale=None, q_start=0):
+    """Differentiable O = softmax(Q K^T * scale [causal]) V for PyTorch training code.
+
+    q [B, H, Nq, d], k and v [B, H, Nk, d], contiguous bf16 CUDA tensors; returns O
+    [B, H, Nq, d] bf16.  Calling ``backward`` on anything computed from O runs
+    fa_backward and leaves bf16 gradients in ``q.grad``, ``k.grad`` and ``v.grad``.
+    """
+    return _FlashAttention.apply(q, k, v, bool(causal), scale, int(q_start))
