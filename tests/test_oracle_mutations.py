@@ -139,6 +139,12 @@ MUTATIONS = [
     ("key-major: old sum not repaired", "r_new = conv_old * r_old + conv_new * r_t", "r_new = r_old + conv_new * r_t"),
     ("key-major: blend not diluted", "c = np.where(r_new > 0, conv_old * r_old / safe, 0.0)", "c = np.where(r_new > 0, conv_old, 0.0)"),
     ("key-major: newcomer not converted", "pour = conv_new[:, None] * (p_t @ v[j0:j1]) / safe[:, None]", "pour = (p_t @ v[j0:j1]) / safe[:, None]"),
+    ("dense backward: dQ without scale", "dq[h][r0:r1] = (ds @ k[h]) * sc", "dq[h][r0:r1] = ds @ k[h]"),
+    ("dense backward: dV from P not P^T", "dv[h] += p.T @ do_rows", "dv[h] += p[:, :do_rows.shape[0]].T @ do_rows[:p.shape[0]]"),
+    ("tiled: rescale sign flipped", "alpha = np.exp(m - m_new) if l > 0.0 else 0.0", "alpha = np.exp(m_new - m) if l > 0.0 else 0.0"),
+    ("tiled: LSE in base 2", "lse[i] = m + np.log(l)", "lse[i] = m + np.log2(l)"),
+    ("tiled: exponent not shifted by the max", "e = np.exp(s - m_new)", "e = np.exp(s) * 0 + np.exp(s - m)"),
+    ("tiled backward: dQ without scale", "dq[i] += (ds @ k[start:stop]) * sc", "dq[i] += ds @ k[start:stop]"),
     ("mask ignores q_start", "qpos = np.arange(q_start, q_start + nq)[:, None]", "qpos = np.arange(0, nq)[:, None]"),
     ("dense backward ignores q_start", "_, _, p = _dense_rows(q_rows, k[h], v[h], sc, causal, q_start + r0)",
      "_, _, p = _dense_rows(q_rows, k[h], v[h], sc, causal, r0)"),
