@@ -104,9 +104,20 @@ def _pins_pass(o) -> bool:
         qd, kd, vd = rng.normal(size=(1, 8)), rng.normal(size=(13, 8)), rng.normal(size=(13, 8))
         ref_o, ref_l = o.attention_dense(qd, kd, vd)
         for n_split in (1, 3, 20):
-            dec_o, dec_l, _ = o.attention_split_decode(qd, kd, vd, n_split)
+            dec_o, dec_l, parts = o.attention_split_decode(qd, kd, vd, n_split)
             np.testing.assert_allclose(dec_o, ref_o, atol=1e-12)
             np.testing.assert_allclose(dec_l, ref_l, atol=1e-12)
+            bounds = o.split_bounds(13, n_split)
+            for si, part in enumerate(parts):  # an empty segment is the identity (-inf, 0, 0)
+                if bounds[si + 1] == bounds[si]:
+                    assert np.all(np.isneginf(part.m)) and np.all(part.l == 0) and np.all(part.o == 0)
+        # a state's m is its run's max; merging two empty states gives the empty state
+        sc = rng.normal(scale=3.0, size=(3, 10))
+        st = o.state_of_scores(sc, rng.normal(size=(10, 4)))
+        np.testing.assert_array_equal(st.m, sc.max(axis=1))
+        e = o.empty_state((3,), 4)
+        ee = o.merge_states(e, e)
+        assert np.all(np.isneginf(ee.m)) and np.all(ee.l == 0) and np.all(ee.o == 0)
     except (AssertionError, ValueError, FloatingPointError):
         return False
     return True
@@ -145,6 +156,10 @@ MUTATIONS = [
     ("tiled: LSE in base 2", "lse[i] = m + np.log(l)", "lse[i] = m + np.log2(l)"),
     ("tiled: exponent not shifted by the max", "e = np.exp(s - m_new)", "e = np.exp(s) * 0 + np.exp(s - m)"),
     ("tiled backward: dQ without scale", "dq[i] += (ds @ k[start:stop]) * sc", "dq[i] += ds @ k[start:stop]"),
+    ("state: m from the first score", "m = s.max(axis=-1)", "m = s[..., 0]"),
+    ("decode: empty segment given a zero max", "parts.append(empty_state(q.shape[:-1], v.shape[-1]))",
+     "parts.append(SoftmaxState(np.zeros(q.shape[:-1]), np.zeros(q.shape[:-1]), np.zeros(q.shape[:-1] + (v.shape[-1],))))"),
+    ("merge: guarded base dropped", "return np.where(np.isinf(m), 0.0, m)", "return m"),
     ("mask ignores q_start", "qpos = np.arange(q_start, q_start + nq)[:, None]", "qpos = np.arange(0, nq)[:, None]"),
     ("dense backward ignores q_start", "_, _, p = _dense_rows(q_rows, k[h], v[h], sc, causal, q_start + r0)",
      "_, _, p = _dense_rows(q_rows, k[h], v[h], sc, causal, r0)"),
