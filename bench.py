@@ -172,6 +172,62 @@ def max_over_ranks(x, world):
     return float(t.item())
 
 
+# ----------------------------------------------------------------------------- bars of the path
+O_MAX_ABS, LSE_MAX_ABS, GRAD_REL_FRO = 1e-2, 2e-3, 2e-2
+
+
+def _bf16_half_ulp(x):
+    """Half a bf16 ulp at |x| (8 significant bits): the storage rounding of a bf16 output."""
+    import numpy as np
+
+    x = np.abs(np.asarray(x, dtype=np.float64))
+    return 2.0 ** (np.floor(np.log2(np.maximum(x, 2.0 ** -126))) - 8)
+
+
+def _rel_fro(got, ref):
+    import numpy as np
+
+    den = np.linalg.norm(ref)
+    return float(np.linalg.norm(got - ref) / den) if den > 0 else float(np.linalg.norm(got))
+
+
+def oracle_parity(samples):
+    """The cpu_baseline leg: the float64 oracle on each workload's sample (heads of the
+    very inputs the GPU ran, with the GPU's outputs for them), timed, and the GPU's
+    errors against it at the path's bars (O max-abs 1e-2, plus bf16's half-ulp for a
+    bf16 output; LSE max-abs 2e-3; dQ, dK, dV relative Frobenius 2e-2)."""
+    import numpy as np
+
+    from oracle import attention_dense, attention_dense_backward, attention_split_decode
+
+    out = {}
+    for name, smp in samples.items():
+        x, g = smp["inputs"], smp["gpu"]
+        t0 = time.perf_counter()
+        if smp["kind"] == "decode":
+            ref_o, ref_l, _ = attention_split_decode(x["q"], x["k"], x["v"], smp["n_split"])
+            ref_l = ref_l[..., 0]
+            grads = None
+        else:
+            ref_o, ref_l = attention_dense(x["q"], x["k"], x["v"], causal=smp["causal"])
+            grads = (attention_dense_backward(x["q"], x["k"], x["v"], x["do"], causal=smp["causal"])
+                     if "do" in x else None)
+        secs = time.perf_counter() - t0
+        err_o = np.abs(g["o"] - ref_o)
+        bar = O_MAX_ABS + (_bf16_half_ulp(ref_o) if smp["o_dtype"] == "bf16" else 0.0)
+        par = {"subset": smp["subset"], "o_dtype": smp["o_dtype"], "o_max_abs": float(err_o.max()),
+               "o_excess_over_bar": float((err_o - bar).max()), "lse_max_abs": float(np.abs(g["lse"] - ref_l).max())}
+        ok = par["o_excess_over_bar"] <= 0 and par["lse_max_abs"] <= LSE_MAX_ABS
+        if grads is not None:
+            for gname, ref in zip(("dq", "dk", "dv"), grads):
+                par[gname + "_rel_fro"] = _rel_fro(g[gname], ref)
+                ok = ok and par[gname + "_rel_fro"] <= GRAD_REL_FRO
+        par["within_bars"] = bool(ok)
+        par["oracle_seconds"] = secs
+        out[name] = par
+    return out
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 def oracle_sample(w_fb, w_dec, n_heads_fb, n_heads_dec):
     """Run the float64 oracle on `n_heads` heads of each workload; return
@@ -325,9 +381,108 @@ def run_reference(args, world, rank):
 
 
 # ----------------------------------------------------------------------------- GPU path
+def _time_alone(fn, reps, flush, stream):
+    """Median and best of `reps` CUDA-event timings of fn() on `stream`, after 3
+    warm-up calls, with L2 flushed (a 256 MB write) before each timed call."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        fn()
+    times = []
+    for _ in range(reps):
+        flush.zero_()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return statistics.median(times), min(times)
+
+
+def _rate_record(med_ms, best_ms, work, unit, peaks, reps):
+    scale = 1e12 if unit == "TFLOP/s" else 1e9
+    r = {"median_ms": med_ms, "best_ms": best_ms, "reps": reps, "unit": unit, "rate": work / (med_ms * 1e-3) / scale,
+         "best_rate": work / (best_ms * 1e-3) / scale}
+    if unit == "TFLOP/s":
+        r["frac_of_bf16_peak"] = r["rate"] / peaks["bf16_tflops"]
+        r["frac_of_bf16_sustained"] = r["rate"] / peaks["bf16_tflops_sustained"]
+    else:
+        r["frac_of_hbm_peak"] = r["rate"] / peaks["hbm_gbs"]
+        r["frac_of_8tbs"] = r["rate"] / 8000.0
+    return r
+
+
+def _f64(t):
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+def workload_records(peaks, reps, dev, stream, keep_samples):
+    """Every named workload's kernels, each timed alone (median and best of `reps`,
+    L2 flushed before each call), with the GPU's outputs for a few heads kept (as
+    float64 host arrays, inputs alongside) for the oracle leg's parity check."""
+    from exact_attention_flash_gb300 import (backward_workspace_bytes, decode_workspace_bytes, fa_backward,
+                                             fa_decode, fa_forward, forward_workspace_bytes)
+    from exact_attention_flash_gb300.workloads import WORKLOADS, make_inputs
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    recs, samples = {}, {}
+    for name, w in WORKLOADS.items():
+        if w.kind == "decode":
+            q, k, v = make_inputs(w, dev)
+            ws = torch.empty(decode_workspace_bytes(w.B, w.H, w.d, w.n_split), device=dev, dtype=torch.uint8)
+            o = torch.empty((w.B, w.H, 1, w.d), device=dev)
+            lse = torch.empty((w.B, w.H), device=dev)
+            med, best = _time_alone(lambda: fa_decode(q, k, v, w.n_split, workspace=ws, out=o, lse=lse, stream=stream),
+                                    reps, flush, stream)
+            recs[name] = {"B": w.B, "H": w.H, "L": w.N, "d": w.d, "n_split": w.n_split, "kernels": {
+                "decode": _rate_record(med, best, decode_bytes(w.B, w.H, w.N, w.d, w.n_split), "GB/s", peaks, reps)}}
+            heads = [(0, 0), (0, 31), (3, 7), (7, 16), (9, 1), (12, 30), (15, 0), (15, 31)]
+            if keep_samples:
+                pick = lambda t: _f64(torch.stack([t[b, h] for b, h in heads]))  # noqa: E731
+                samples[name] = {"kind": "decode", "n_split": w.n_split, "o_dtype": "f32",
+                                 "subset": f"{len(heads)} of {w.B * w.H} heads",
+                                 "inputs": {"q": pick(q), "k": pick(k), "v": pick(v)},
+                                 "gpu": {"o": pick(o), "lse": _f64(torch.stack([lse[b, h:h + 1] for b, h in heads]))}}
+            del q, k, v, ws, o, lse
+        else:
+            q, k, v, do = make_inputs(w, dev)
+            odt = torch.float32 if w.out_f32 else torch.bfloat16
+            o = torch.empty(q.shape, device=dev, dtype=odt)
+            lse = torch.empty((w.B, w.H, w.N), device=dev)
+            wsf = torch.empty(forward_workspace_bytes(w.B, w.H, w.N, w.d, w.causal), device=dev, dtype=torch.uint8)
+            fwd = lambda: fa_forward(q, k, v, causal=w.causal, out=o, lse=lse, workspace=wsf, stream=stream)  # noqa: E731
+            med, best = _time_alone(fwd, reps, flush, stream)
+            kern = {"forward": _rate_record(med, best, attention_flops(w.B, w.H, w.N, w.d, w.causal, False),
+                                            "TFLOP/s", peaks, reps)}
+            grads = None
+            if w.backward:
+                grads = [torch.empty(q.shape, device=dev) for _ in range(3)]
+                wsb = torch.empty(backward_workspace_bytes(w.B, w.H, w.N, w.d), device=dev, dtype=torch.uint8)
+                bwd = lambda: fa_backward(q, k, v, o, lse, do, causal=w.causal, workspace=wsb,  # noqa: E731
+                                          dq=grads[0], dk=grads[1], dv=grads[2], stream=stream)
+                med, best = _time_alone(bwd, reps, flush, stream)
+                kern["backward"] = _rate_record(med, best, attention_flops(w.B, w.H, w.N, w.d, w.causal, True),
+                                                "TFLOP/s", peaks, reps)
+            recs[name] = {"B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal, "qk_mult": w.qk_mult,
+                          "o_dtype": "f32" if w.out_f32 else "bf16", "kernels": kern}
+            if w.B * w.H == 1:
+                recs[name]["note"] = "one (batch, head): two CTAs of 128 rows, launch-latency bound"
+            if keep_samples:
+                x = {"q": _f64(q[0, 0]), "k": _f64(k[0, 0]), "v": _f64(v[0, 0])}
+                g = {"o": _f64(o[0, 0]), "lse": _f64(lse[0, 0])}
+                if grads is not None:
+                    x["do"] = _f64(do[0, 0])
+                    g.update(dq=_f64(grads[0][0, 0]), dk=_f64(grads[1][0, 0]), dv=_f64(grads[2][0, 0]))
+                samples[name] = {"kind": "attention", "causal": w.causal, "o_dtype": recs[name]["o_dtype"],
+                                 "subset": f"head (0, 0) of {w.B * w.H}", "inputs": x, "gpu": g}
+            del q, k, v, do, o, lse, wsf, grads
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+    return recs, samples
+
+
 def run_ours(args, world, rank, local):
     from exact_attention_flash_gb300 import (_lib, backward_workspace_bytes, decode_workspace_bytes, fa_backward,
-                                             fa_decode, fa_device_status, fa_forward)
+                                             fa_decode, fa_device_status, fa_forward, forward_workspace_bytes)
     from exact_attention_flash_gb300.build import build
     from exact_attention_flash_gb300.workloads import WORKLOADS, make_inputs
 
@@ -344,6 +499,7 @@ def run_ours(args, world, rank, local):
     dq = torch.empty(q.shape, device=dev, dtype=torch.float32)
     dk = torch.empty_like(dq)
     dv = torch.empty_like(dq)
+    ws_f = torch.empty(forward_workspace_bytes(w.B, w.H, w.N, w.d, True), device=dev, dtype=torch.uint8)
     ws_b = torch.empty(backward_workspace_bytes(w.B, w.H, w.N, w.d), device=dev, dtype=torch.uint8)
     od = torch.empty((wd.B, wd.H, 1, wd.d), device=dev, dtype=torch.float32)
     lsed = torch.empty((wd.B, wd.H), device=dev, dtype=torch.float32)
@@ -351,7 +507,7 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
 
     def fwd():
-        fa_forward(q, k, v, causal=True, out=o, lse=lse, stream=stream)
+        fa_forward(q, k, v, causal=True, out=o, lse=lse, workspace=ws_f, stream=stream)
 
     def bwd():
         fa_backward(q, k, v, o, lse, do, causal=True, workspace=ws_b, dq=dq, dk=dk, dv=dv, stream=stream)
@@ -391,10 +547,11 @@ def run_ours(args, world, rank, local):
     t_bwd = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]
     t_dec = [ev[i][2].elapsed_time(ev[i][3]) for i in range(n)]
     t_step = [ev[i][0].elapsed_time(ev[i][3]) for i in range(n)]
-    fwd_ms = max_over_ranks(sum(t_fwd) / n, world)
-    bwd_ms = max_over_ranks(sum(t_bwd) / n, world)
-    dec_ms = max_over_ranks(sum(t_dec) / n, world)
-    step_ms = max_over_ranks(sum(t_step) / n, world)
+    # Medians over the timed steps (best and mean alongside); max over ranks.
+    fwd_ms = max_over_ranks(statistics.median(t_fwd), world)
+    bwd_ms = max_over_ranks(statistics.median(t_bwd), world)
+    dec_ms = max_over_ranks(statistics.median(t_dec), world)
+    step_ms = max_over_ranks(statistics.median(t_step), world)
 
     f_fwd = attention_flops(w.B, w.H, w.N, w.d, True, False)
     f_bwd = attention_flops(w.B, w.H, w.N, w.d, True, True)
@@ -445,7 +602,7 @@ def run_ours(args, world, rank, local):
                     stream.wait_event(copied[b])
                 x = dev_in[b]
                 ob, lb, dqb, dkb, dvb = dev_out[b]
-                fa_forward(x[0], x[1], x[2], causal=True, out=ob, lse=lb, stream=stream)
+                fa_forward(x[0], x[1], x[2], causal=True, out=ob, lse=lb, workspace=ws_f, stream=stream)
                 fa_backward(x[0], x[1], x[2], ob, lb, x[3], causal=True, workspace=ws, dq=dqb, dk=dkb, dv=dvb,
                             stream=stream, grad_dtype=grad_dtype)
                 computed[b] = torch.cuda.Event()
@@ -476,13 +633,42 @@ def run_ours(args, world, rank, local):
 
     e2e_value, d2h = e2e_measure(torch.float32)
     e2e16_value, d2h16 = e2e_measure(torch.bfloat16)
+    if fa_device_status() != 0:
+        raise RuntimeError("device status not clean after the end-to-end steps")
+
+    # ---- every named workload, each kernel timed alone; the oracle leg (cpu_baseline)
+    # checks the GPU's outputs on a few heads of each.
+    del host_in, dev_in
+    torch.cuda.empty_cache()
+    want_oracle = rank == 0 and world == 1 and not args.no_cpu_baseline
+    per_workload, samples = workload_records(peaks, max(args.reps, 20), dev, stream, keep_samples=want_oracle)
+    if fa_device_status() != 0:
+        raise RuntimeError("device status not clean after the per-workload timings")
 
     if rank != 0:
         return
     bwd_tflops = f_bwd / (bwd_ms * 1e-3) / 1e12
     fwd_tflops = f_fwd / (fwd_ms * 1e-3) / 1e12
     dec_gbs = dbytes / (dec_ms * 1e-3) / 1e9
-    cpu = cpu_baseline_record(heads_fb=1, heads_dec=8) if (world == 1 and not args.no_cpu_baseline) else None
+    cpu = None
+    if want_oracle:
+        parity = oracle_parity(samples)
+        for name, par in parity.items():
+            per_workload[name]["parity"] = par
+        fb, dc = parity[FWD_BWD], parity[DECODE]
+        fb_flops = attention_flops(1, 1, w.N, w.d, True, False) + attention_flops(1, 1, w.N, w.d, True, True)
+        dc_bytes = decode_bytes(1, 8, wd.N, wd.d, wd.n_split)
+        cpu = {"value": fb_flops / fb["oracle_seconds"] / 1e12, "unit": "TFLOP/s", "cores": _NCORES, "kind": "oracle",
+               "sample": f"head (0, 0) of {FWD_BWD} (dense forward + backward, float64 numpy, "
+                         f"{fb['oracle_seconds']:.2f} s); decode: {dc['subset']} of {DECODE} "
+                         f"({dc['oracle_seconds']:.2f} s, {dc_bytes / dc['oracle_seconds'] / 1e9:.3f} GB/s); "
+                         "the same runs give each workload's parity errors",
+               "seconds": sum(p["oracle_seconds"] for p in parity.values()),
+               "decode_gbs": dc_bytes / dc["oracle_seconds"] / 1e9}
+
+    def step_kernel(ts, ms):
+        return {"median_ms": ms, "best_ms": min(ts), "mean_ms": sum(ts) / len(ts)}
+
     line = {
         "metric": METRIC,
         "value": value,
@@ -497,28 +683,34 @@ def run_ours(args, world, rank, local):
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1), bf16; Q,K x8)",
         "config": {"workload": FWD_BWD, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": True,
-                   "decode_workload": DECODE, "l2": "inputs larger than L2 (K/V stream of 8.6 GB per step)",
-                   "parallelism": f"replicas x{world}"},
+                   "decode_workload": DECODE, "l2": "inputs larger than L2 (K/V stream of 8.6 GB per step); "
+                   "the per-workload timings flush L2 before each call",
+                   "timing": "medians over the timed steps", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "kernel": "fa_backward (preprocess + bwd_kernel)", "achieved": bwd_tflops,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": bwd_tflops / peaks["bf16_tflops"],
                      "traffic": recorded_traffic("fa_bwd.cu", "bwd_kernel_d128_causal"),
                      "peak_source": peaks["source"] + " burst"},
         "kernels": {
-            "forward": {"ms": fwd_ms, "tflops": fwd_tflops, "frac_of_bf16_peak": fwd_tflops / peaks["bf16_tflops"],
+            "forward": {**step_kernel(t_fwd, fwd_ms), "ms": fwd_ms, "tflops": fwd_tflops,
+                        "frac_of_bf16_peak": fwd_tflops / peaks["bf16_tflops"],
                         "frac_of_bf16_sustained": fwd_tflops / peaks["bf16_tflops_sustained"],
                         "traffic": recorded_traffic("fa_fwd.cu", "fwd_kernel_d128_causal")},
-            "backward": {"ms": bwd_ms, "tflops": bwd_tflops, "frac_of_bf16_peak": bwd_tflops / peaks["bf16_tflops"],
+            "backward": {**step_kernel(t_bwd, bwd_ms), "ms": bwd_ms, "tflops": bwd_tflops,
+                         "frac_of_bf16_peak": bwd_tflops / peaks["bf16_tflops"],
                          "frac_of_bf16_sustained": bwd_tflops / peaks["bf16_tflops_sustained"]},
-            "decode": {"ms": dec_ms, "gbs": dec_gbs, "bound": "hbm", "peak_gbs": peaks["hbm_gbs"],
-                       "frac_of_hbm_peak": dec_gbs / peaks["hbm_gbs"], "frac_of_8tbs": dec_gbs / 8000.0,
-                       "algorithmic_bytes": dbytes,
+            "decode": {**step_kernel(t_dec, dec_ms), "ms": dec_ms, "gbs": dec_gbs, "bound": "hbm",
+                       "peak_gbs": peaks["hbm_gbs"], "frac_of_hbm_peak": dec_gbs / peaks["hbm_gbs"],
+                       "frac_of_8tbs": dec_gbs / 8000.0, "algorithmic_bytes": dbytes,
                        "traffic": recorded_traffic("fa_decode.cu", "decode_split_kernel_d128")},
         },
+        "workloads": per_workload,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "grad_dtype": "f32"},
         # the same pipeline with the gradients returned as bf16 (fp32 accumulation inside)
         "e2e_bf16_grads": {"value": e2e16_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                            "d2h_bytes_per_step": d2h16},
+        # this library's kernels per timed step: fwd_kernel, bwd_preprocess + bwd_kernel,
+        # decode_split_kernel (the forward's and the decode's counter clears are runtime memsets)
         "gpu_launches": 4 * n,
         "clocks": clocks,
         "cpu_baseline": cpu,

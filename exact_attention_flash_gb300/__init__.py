@@ -14,8 +14,8 @@ import torch
 from . import _lib
 from ._lib import FAError
 
-__all__ = ["flash_attention", "fa_forward", "fa_backward", "fa_decode", "fa_device_status", "FAError",
-           "backward_workspace_bytes",
+__all__ = ["flash_attention", "fa_forward", "fa_backward", "fa_decode", "fa_device_status", "fa_get_device_status",
+           "FAError", "forward_workspace_bytes", "backward_workspace_bytes",
            "decode_workspace_bytes", "fa_set_stats", "stats_counters", "STATS_FIELDS", "fa_merge_states",
            "decode_auto_split", "fa_forward_keymajor"]
 
@@ -54,19 +54,32 @@ def _scale_arg(scale):
     return 0.0 if scale is None else float(scale)
 
 
+def _check_workspace(t):
+    if not t.is_cuda or t.dtype != torch.uint8 or not t.is_contiguous():
+        raise ValueError("workspace must be a contiguous uint8 CUDA tensor")
+
+
 def _check_out(name, t, shape, dtypes):
     if not t.is_cuda or t.dtype not in dtypes or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} must be a contiguous CUDA tensor of shape {tuple(shape)} and dtype in {dtypes}")
 
 
+def forward_workspace_bytes(B, H, N, d, causal=False) -> int:
+    """Workspace bytes of :func:`fa_forward` (the persistent grid's work counter)."""
+    return int(_lib.load().fa_forward_workspace_size(B, H, N, d, int(bool(causal))))
+
+
 @_on_tensor_device
 def fa_forward(q, k, v, causal=False, scale=None, out_dtype=torch.bfloat16, precise=False, out=None, lse=None,
-               stream=None, q_start=0):
+               stream=None, q_start=0, workspace=None):
     """O, LSE = softmax(Q K^T * scale [causal]) V.
 
     q [B, H, Nq, d], k and v [B, H, Nk, d], bf16.  Query row i sits at position
     q_start + i; with ``causal`` it sees the keys j <= q_start + i.  Nq = Nk with
-    q_start = 0 is ordinary self-attention.
+    q_start = 0 is ordinary self-attention.  ``workspace``: a uint8 CUDA tensor of
+    at least :func:`forward_workspace_bytes`; one is allocated when None.  Calls
+    whose GPU work overlaps (other streams, graphs replayed at once) need
+    workspaces of their own.
     """
     lib = _lib.load()
     _check_bf16("q", q)
@@ -82,10 +95,13 @@ def fa_forward(q, k, v, causal=False, scale=None, out_dtype=torch.bfloat16, prec
     if lse is None:
         lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
     _check_out("lse", lse, (B, H, Nq), (torch.float32,))
+    if workspace is None:
+        workspace = torch.empty(forward_workspace_bytes(B, H, Nq, d, causal), device=q.device, dtype=torch.uint8)
+    _check_workspace(workspace)
     o_code = _lib.FA_F32 if out.dtype == torch.float32 else _lib.FA_BF16
     code = lib.fa_forward_qk(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), o_code, lse.data_ptr(),
                              B, H, Nq, Nk, int(q_start), d, _scale_arg(scale), int(bool(causal)), int(bool(precise)),
-                             _stream_ptr(stream))
+                             workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
     _lib.check("fa_forward_qk", code)
     return out, lse
 
@@ -188,9 +204,12 @@ def fa_decode(q, k, v, n_split=None, scale=None, return_partials=False, workspac
     return (out, lse, parts) if return_partials else (out, lse)
 
 
-def fa_device_status(stream=None) -> int:
+def fa_get_device_status(stream=None) -> int:
     """Synchronise and return (and clear) the kernels' device status as an fa_status code."""
-    return int(_lib.load().fa_device_status(_stream_ptr(stream)))
+    return int(_lib.load().fa_get_device_status(_stream_ptr(stream)))
+
+
+fa_device_status = fa_get_device_status
 
 
 def fa_set_stats(counters=None) -> None:

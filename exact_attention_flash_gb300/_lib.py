@@ -36,14 +36,16 @@ _Z = ctypes.c_size_t
 SIGNATURES = {
     "fa_abi_version": (_I, []),
     "fa_status_string": (ctypes.c_char_p, [_I]),
-    "fa_forward": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _F, _I, _I, _P]),
-    "fa_forward_qk": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "fa_forward_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "fa_forward": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _F, _I, _I, _P, _Z, _P]),
+    "fa_forward_qk": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _F, _I, _I, _P, _Z, _P]),
     "fa_backward_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
     "fa_backward_qk": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
     "fa_backward": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
     "fa_decode_workspace_size": (_Z, [_I, _I, _I, _I]),
     "fa_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _Z, _P]),
     "fa_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P]),
+    "fa_get_device_status": (_I, [_P]),
     "fa_device_status": (_I, [_P]),
     "fa_set_stats": (_I, [_P]),
     "fa_merge_states": (_I, [_P, _P, _P, _P, _P, _P, _I, ctypes.c_longlong, _I, _P]),
@@ -51,6 +53,7 @@ SIGNATURES = {
     "fa_forward_keymajor": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
     "fa_decode_auto_split": (_I, [_I, _I, _I]),
     "fa_debug_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
+    "fa_debug_next_wait_limit": (_I, [ctypes.c_ulonglong]),
 }
 
 _lib = None

@@ -97,7 +97,42 @@ size_t backward_bias_bytes(int B, int H, int N) {
 // Counters set by fa_set_stats for the calling host thread's calls (null: none).
 thread_local unsigned long long* t_stats = nullptr;
 
+// Wait limit for the calling host thread's next forward or backward call, set by
+// fa_debug_next_wait_limit; taken (and cleared) by that one call.
+thread_local bool t_next_wait_set = false;
+thread_local unsigned long long t_next_wait_ns = 0;
+
+unsigned long long take_wait_limit() {
+  const unsigned long long ns = t_next_wait_set ? t_next_wait_ns : fa::kDefaultWaitNs;
+  t_next_wait_set = false;
+  return ns;
+}
+
+// The forward's workspace: one 32-bit work counter, padded.
+constexpr size_t kForwardWorkspaceBytes = 256;
+
 }  // namespace
+
+namespace fa {
+
+// Argument checks shared by fa_decode and fa_decode_noalloc, in one place so that
+// the two entry points cannot drift apart: pointers, sizes, and the workspace the
+// call needs, fa_decode_workspace_size(B, H, d, n_split), against `workspace_bytes`
+// (the caller's workspace, or the fixed scratch array).  No CUDA call.
+fa_status check_decode_args(const void* q, const void* k, const void* v, const float* o, const float* lse, int B,
+                            int H, int L, int d, int n_split, size_t workspace_bytes) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return FA_ERR_INVALID_ARG;
+  if (n_split < 1 || L < 1 || B < 1 || H < 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (B > 65535 || H > 65535 || n_split > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  const size_t need = fa_decode_workspace_size(B, H, d, n_split);
+  if (need == 0) return FA_ERR_UNSUPPORTED;  // beyond any device's memory
+  if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+  return FA_OK;
+}
+
+}  // namespace fa
 
 extern "C" {
 
@@ -116,20 +151,30 @@ const char* fa_status_string(fa_status s) {
   return "unknown status";
 }
 
+size_t fa_forward_workspace_size(int B, int H, int N, int d, int causal) {
+  (void)causal;
+  if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+  return kForwardWorkspaceBytes;
+}
+
 fa_status fa_forward(const void* q, const void* k, const void* v, void* o, fa_dtype o_dtype, float* lse, int B,
-                     int H, int N, int d, float scale, int causal, int precise, void* stream) {
-  return fa_forward_qk(q, k, v, o, o_dtype, lse, B, H, N, N, 0, d, scale, causal, precise, stream);
+                     int H, int N, int d, float scale, int causal, int precise, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  return fa_forward_qk(q, k, v, o, o_dtype, lse, B, H, N, N, 0, d, scale, causal, precise, workspace,
+                       workspace_bytes, stream);
 }
 
 fa_status fa_forward_qk(const void* q, const void* k, const void* v, void* o, fa_dtype o_dtype, float* lse, int B,
                         int H, int Nq, int Nk, int q_start, int d, float scale, int causal, int precise,
-                        void* stream) {
+                        void* workspace, size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
   if (o_dtype != FA_BF16 && o_dtype != FA_F32) return FA_ERR_INVALID_ARG;
   fa_status st = check_lengths(B, H, Nq, Nk, q_start, d);
   if (st != FA_OK) return st;
   if (static_cast<long long>(B) * H * ((Nq + 255) / 256) > kMaxCount) return FA_ERR_UNSUPPORTED;  // work items
+  if (!workspace || !aligned16(workspace) || workspace_bytes < kForwardWorkspaceBytes) return FA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   fa::ForwardArgs a{};
   const int BH = B * H;
   if ((st = make_row_tile_map(&a.tm_q, q, BH, Nq, d)) != FA_OK) return st;
@@ -149,7 +194,12 @@ fa_status fa_forward_qk(const void* q, const void* k, const void* v, void* o, fa
   a.o_f32 = (o_dtype == FA_F32) ? 1 : 0;
   a.precise = precise ? 1 : 0;
   a.stats = t_stats;
-  return fa::launch_forward(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  a.wait_ns = take_wait_limit();
+  // The persistent grid claims its work items from this counter: zero it first,
+  // in stream order, so that the workspace needs no initialisation by the caller.
+  a.sched = static_cast<unsigned*>(workspace);
+  if (cudaMemsetAsync(a.sched, 0, sizeof(unsigned), s) != cudaSuccess) return FA_ERR_CUDA;
+  return fa::launch_forward(a, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 // Per query row over [B*H, N rounded up to 64]: two 32-byte rows of the bias tiles
@@ -221,28 +271,32 @@ fa_status fa_backward_qk(const void* q, const void* k, const void* v, const void
   a.head_group = fa::head_group_for(a.causal, 2ll * Nq * d * 2 + static_cast<long long>(Nq) * d * 4, B * H);  // Q, dO, dQ
   a.o_f32 = (o_dtype == FA_F32) ? 1 : 0;
   a.stats = t_stats;
+  a.wait_ns = take_wait_limit();
   const cudaError_t e = fa::launch_backward(a, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// Every count is checked before it is multiplied: the segment states take
+// B * H * n_split * (d + 2) floats, and a product that would pass 2^62 bytes
+// (far beyond any device) is reported as 0, never wrapped around.
 size_t fa_decode_workspace_size(int B, int H, int d, int n_split) {
   if (B < 1 || H < 1 || n_split < 1 || d < 1) return 0;
-  const size_t counters = round_up(static_cast<size_t>(B) * H * sizeof(unsigned), 256);
-  const size_t partials = static_cast<size_t>(B) * H * n_split * (d + 2) * sizeof(float);
+  constexpr size_t kLimit = size_t(1) << 62;
+  const size_t heads = static_cast<size_t>(B) * static_cast<size_t>(H);  // < 2^62
+  const size_t state_bytes = (static_cast<size_t>(d) + 2) * sizeof(float);
+  if (heads > kLimit / static_cast<size_t>(n_split) || heads * n_split > kLimit / state_bytes) return 0;
+  const size_t counters = round_up(heads * sizeof(unsigned), 256);
+  const size_t partials = heads * n_split * state_bytes;
   return counters + round_up(partials, 256);
 }
 
 fa_status fa_decode(const void* q, const void* k, const void* v, float* o, float* lse, int B, int H, int L, int d,
                     float scale, int n_split, float* partials, void* workspace, size_t workspace_bytes,
                     void* stream) {
-  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return FA_ERR_INVALID_ARG;
-  if (n_split < 1 || L < 1 || B < 1 || H < 1) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (B > 65535 || H > 65535 || n_split > (1 << 30)) return FA_ERR_UNSUPPORTED;
-  if (!workspace || !aligned16(workspace) || workspace_bytes < fa_decode_workspace_size(B, H, d, n_split))
-    return FA_ERR_WORKSPACE;
+  fa_status st = fa::check_decode_args(q, k, v, o, lse, B, H, L, d, n_split, workspace_bytes);
+  if (st != FA_OK) return st;
+  if (!workspace || !aligned16(workspace)) return FA_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t counter_bytes = round_up(static_cast<size_t>(B) * H * sizeof(unsigned), 256);
   fa::DecodeArgs a{};
@@ -303,7 +357,7 @@ fa_status fa_forward_keymajor(const void* q, const void* k, const void* v, void*
   return fa::launch_forward_keymajor(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-fa_status fa_device_status(void* stream) {
+fa_status fa_get_device_status(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned f = 0, b = 0, dcd = 0, km = 0, mg = 0;
   if (fa::read_clear_forward_status(&f, s) != cudaSuccess) return FA_ERR_CUDA;
@@ -347,6 +401,15 @@ int fa_decode_auto_split(int B, int H, int L) {
 fa_status fa_set_stats(unsigned long long* counters) {
   if ((reinterpret_cast<uintptr_t>(counters) & 7u) != 0) return FA_ERR_INVALID_ARG;
   t_stats = counters;
+  return FA_OK;
+}
+
+fa_status fa_device_status(void* stream) { return fa_get_device_status(stream); }
+
+fa_status fa_debug_next_wait_limit(unsigned long long limit_ns) {
+  if (limit_ns > 5000000000ull) return FA_ERR_INVALID_ARG;
+  t_next_wait_ns = limit_ns;
+  t_next_wait_set = true;
   return FA_OK;
 }
 

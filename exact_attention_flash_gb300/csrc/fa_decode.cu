@@ -291,37 +291,16 @@ cudaError_t static_scratch_for_current_device(void** out) {
 extern "C" fa_status fa_decode_noalloc(const void* q, const void* k, const void* v, float* o, float* lse, int B,
                                        int H, int L, int d, float scale, int n_split, float* partials,
                                        void* stream) {
-  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-  const auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
-  if (misaligned(q) || misaligned(k) || misaligned(v)) return FA_ERR_INVALID_ARG;
-  if (n_split < 1 || L < 1 || B < 1 || H < 1) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (B > 65535 || H > 65535 || n_split > (1 << 30)) return FA_ERR_UNSUPPORTED;
-  // Same layout as the fa_decode workspace: counters (256-byte padded), then states.
-  const size_t counter_bytes = (static_cast<size_t>(B) * H * sizeof(unsigned) + 255) / 256 * 256;
-  const size_t state_bytes = static_cast<size_t>(B) * H * n_split * (d + 2) * sizeof(float);
-  if (counter_bytes + state_bytes > static_cast<size_t>(FA_DECODE_NOALLOC_SCRATCH_BYTES)) return FA_ERR_WORKSPACE;
-
+  // The same checks as fa_decode, with the fixed array as the workspace: a call
+  // that needs more than FA_DECODE_NOALLOC_SCRATCH_BYTES returns FA_ERR_WORKSPACE
+  // before any CUDA call.
+  const fa_status st = fa::check_decode_args(q, k, v, o, lse, B, H, L, d, n_split,
+                                             static_cast<size_t>(FA_DECODE_NOALLOC_SCRATCH_BYTES));
+  if (st != FA_OK) return st;
   void* scratch = nullptr;
   if (fa::static_scratch_for_current_device(&scratch) != cudaSuccess) return FA_ERR_CUDA;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  fa::DecodeArgs a{};
-  a.q = q;
-  a.k = k;
-  a.v = v;
-  a.o = o;
-  a.lse = lse;
-  a.partials = partials;
-  a.ws_counters = static_cast<unsigned*>(scratch);
-  a.ws_partials = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) + counter_bytes);
-  a.B = B;
-  a.H = H;
-  a.L = L;
-  a.d = d;
-  a.n_split = n_split;
-  a.scale_log2 = (scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(d))) * 1.4426950408889634f;
-  // The counters must start at zero; the previous call's contents are still there.
-  if (cudaMemsetAsync(a.ws_counters, 0, static_cast<size_t>(B) * H * sizeof(unsigned), s) != cudaSuccess)
-    return FA_ERR_CUDA;
-  return fa::launch_decode(a, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  // fa_decode clears the arrival counters it uses on `stream` (the previous call's
+  // contents are still in the array) and launches on the array's address.
+  return fa_decode(q, k, v, o, lse, B, H, L, d, scale, n_split, partials, scratch,
+                   static_cast<size_t>(FA_DECODE_NOALLOC_SCRATCH_BYTES), stream);
 }

@@ -27,7 +27,6 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -38,14 +37,7 @@ namespace fa {
 namespace {
 
 __device__ unsigned g_fwd_status;
-// Scheduling slots of the persistent forward: {items claimed, CTAs finished}.  Each
-// launch takes the next slot in turn, so launches that overlap on different
-// streams count on different slots; each launch leaves its slot at zero.  Two
-// launches share a slot only if they are kSchedSlots apart in issue order and
-// still run at the same time (a launch captured in a CUDA graph keeps its slot for
-// every replay; replays of one graph run one after another).
-constexpr int kSchedSlots = 4096;
-__device__ unsigned g_fwd_sched[kSchedSlots][2];
+static_assert(kWaitLimitNs == kDefaultWaitNs, "drain waits keep the default pipeline limit");
 
 constexpr int kBM = 128;             // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;             // keys per KV tile
@@ -137,8 +129,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  // Persistent: the producer claims items in dispatch order from a global counter
-  // (whichever CTA is free takes the next, longest first) and passes each index to
+  // Persistent: the producer claims items in dispatch order from a counter in the
+  // caller's workspace (whichever CTA is free takes the next, longest first) and passes each index to
   // the MMA issuer and the softmax warps through a two-slot ring.  The barriers'
   // phases run on across items (one K/V ring, per-tile step counters, one Q and O
   // hand-off per item).
@@ -192,7 +184,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           // Claim the next item and publish it (n_items once none is left).
           const int r = it % kItemRing;
           if (it >= kItemRing &&
-              !mbar_wait(&bars.item_empty[r], ((it / kItemRing) - 1) & 1, &bars.abort, &g_fwd_status))
+              !mbar_wait(&bars.item_empty[r], ((it / kItemRing) - 1) & 1, &bars.abort, &g_fwd_status, a.wait_ns))
             break;
           const unsigned claimed = atomicAdd(a.sched, 1u);
           const int item = claimed < static_cast<unsigned>(n_items) ? static_cast<int>(claimed) : n_items;
@@ -202,7 +194,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           const FwdItem w = fwd_item(a, item);
           // Q tile t is reloaded once the previous item's last S_t product has read it.
           for (int t = 0; ok && t < kTiles; ++t) {
-            if (it > 0 && !mbar_wait(&bars.q_empty[t], (it - 1) & 1, &bars.abort, &g_fwd_status)) {
+            if (it > 0 && !mbar_wait(&bars.q_empty[t], (it - 1) & 1, &bars.abort, &g_fwd_status, a.wait_ns)) {
               ok = false;
               break;
             }
@@ -214,7 +206,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           }
           for (int j = 0; ok && j < w.n_kv[kTiles - 1]; ++j) {
             const int s = g % C::kStages;
-            if (g >= C::kStages && !mbar_wait(&bars.kv_empty[s], ((g / C::kStages) - 1) & 1, &bars.abort, &g_fwd_status)) {
+            if (g >= C::kStages && !mbar_wait(&bars.kv_empty[s], ((g / C::kStages) - 1) & 1, &bars.abort, &g_fwd_status, a.wait_ns)) {
               ok = false;
               break;
             }
@@ -268,12 +260,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           const uint64_t v_d = desc_add(dV, s * C::kTileBytes);
           const uint32_t o_tm = tmem + C::kOCol + t * D, p_tm = tmem + t * kBN;
           const uint32_t acc0 = first ? 0u : 1u;
-          if (!warp_wait(&bars.p_half[t], step & 1, &bars.abort, &g_fwd_status)) return false;
+          if (!warp_wait(&bars.p_half[t], step & 1, &bars.abort, &g_fwd_status, a.wait_ns)) return false;
           tc_fence_after();
   #pragma unroll
           for (int kk = 0; kk < kBN / 32; ++kk)
             umma_ts(o_tm, p_tm + kk * 8, desc_add(v_d, kk * 16 * 128), kIdO, kk > 0 ? 1u : acc0, leader);
-          if (!warp_wait(&bars.p_full[t], step & 1, &bars.abort, &g_fwd_status)) return false;
+          if (!warp_wait(&bars.p_full[t], step & 1, &bars.abort, &g_fwd_status, a.wait_ns)) return false;
           tc_fence_after();
   #pragma unroll
           for (int kk = kBN / 32; kk < kBN / 16; ++kk)
@@ -294,7 +286,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         bool ok = true;
         for (int it = 0; ok; ++it) {
           const int r = it % kItemRing;
-          if (!warp_wait(&bars.item_full[r], (it / kItemRing) & 1, &bars.abort, &g_fwd_status)) break;
+          if (!warp_wait(&bars.item_full[r], (it / kItemRing) & 1, &bars.abort, &g_fwd_status, a.wait_ns)) break;
           const int item = bars.item[r];
           mbar_arrive_warp(&bars.item_empty[r]);
           if (item >= n_items) break;
@@ -306,9 +298,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
               n_skipped += n_kv_total - w.n_kv[t];
             }
           const int s0 = g % C::kStages;
-          ok = warp_wait(&bars.k_full[s0], (g / C::kStages) & 1, &bars.abort, &g_fwd_status);
+          ok = warp_wait(&bars.k_full[s0], (g / C::kStages) & 1, &bars.abort, &g_fwd_status, a.wait_ns);
           for (int t = 0; ok && t < kTiles; ++t) {
-            if (!warp_wait(&bars.q_full[t], it & 1, &bars.abort, &g_fwd_status)) {
+            if (!warp_wait(&bars.q_full[t], it & 1, &bars.abort, &g_fwd_status, a.wait_ns)) {
               ok = false;
               break;
             }
@@ -318,7 +310,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           for (int j = 0; ok && j < w.n_kv[kTiles - 1]; ++j, ++g) {
             const int s = g % C::kStages, sn = (g + 1) % C::kStages;
             const uint32_t phn = ((g + 1) / C::kStages) & 1;
-            if (!warp_wait(&bars.v_full[s], (g / C::kStages) & 1, &bars.abort, &g_fwd_status)) {
+            if (!warp_wait(&bars.v_full[s], (g / C::kStages) & 1, &bars.abort, &g_fwd_status, a.wait_ns)) {
               ok = false;
               break;
             }
@@ -326,7 +318,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
               if (j >= w.n_kv[t]) continue;  // tile 0 may need one key tile fewer
               // The item's first P V_t overwrites O_t: the previous item's epilogue must
               // have read O_t out of tensor memory.
-              if (j == 0 && it > 0 && !warp_wait(&bars.o_empty[t], (it - 1) & 1, &bars.abort, &g_fwd_status)) {
+              if (j == 0 && it > 0 && !warp_wait(&bars.o_empty[t], (it - 1) & 1, &bars.abort, &g_fwd_status, a.wait_ns)) {
                 ok = false;
                 break;
               }
@@ -336,7 +328,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
               }
               if (t == kTiles - 1) umma_commit(&bars.kv_empty[s], leader);
               if (j + 1 < w.n_kv[t]) {
-                if (!warp_wait(&bars.k_full[sn], phn, &bars.abort, &g_fwd_status)) {
+                if (!warp_wait(&bars.k_full[sn], phn, &bars.abort, &g_fwd_status, a.wait_ns)) {
                   ok = false;
                   break;
                 }
@@ -374,7 +366,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     bool ok = true;
     for (int it = 0; ok; ++it) {
     const int ring = it % kItemRing;
-    if (!__all_sync(0xffffffffu, mbar_wait(&bars.item_full[ring], (it / kItemRing) & 1, &bars.abort, &g_fwd_status)))
+    if (!__all_sync(0xffffffffu, mbar_wait(&bars.item_full[ring], (it / kItemRing) & 1, &bars.abort, &g_fwd_status, a.wait_ns)))
       break;
     const int item = bars.item[ring];
     mbar_arrive_warp(&bars.item_empty[ring]);
@@ -388,7 +380,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     float l_hat = 0.f;  // sum of the bf16-rounded p that enter P V: the normaliser of O
     for (int j = 0; j < w.n_kv[t]; ++j, ++step) {
       // Lanes leave together: the TMEM accesses below are warp-collective.
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars.s_full[t], step & 1, &bars.abort, &g_fwd_status))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars.s_full[t], step & 1, &bars.abort, &g_fwd_status, a.wait_ns))) {
         ok = false;
         break;
       }
@@ -502,7 +494,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     // ------------------------------------------------------------ epilogue
     // The whole O row leaves tensor memory first; o_empty then lets the next item's
     // first P V product overwrite it while this row is normalised and stored.
-    if (!ok || !__all_sync(0xffffffffu, mbar_wait(&bars.o_full[t], it & 1, &bars.abort, &g_fwd_status))) {
+    if (!ok || !__all_sync(0xffffffffu, mbar_wait(&bars.o_full[t], it & 1, &bars.abort, &g_fwd_status, a.wait_ns))) {
       ok = false;
       break;
     }
@@ -560,14 +552,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  // The last CTA to finish returns the scheduling slot to zero for its next launch.
-  if (tid == 0) {
-    __threadfence();
-    if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
-      atomicExch(a.sched, 0u);
-      atomicExch(a.sched + 1, 0u);
-    }
-  }
 }
 
 template <int D, bool kPrecise>
@@ -592,13 +576,7 @@ cudaError_t launch_fwd_t(const ForwardArgs& a, cudaStream_t stream) {
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(items < sms ? items : sms));
-  static std::atomic<unsigned> next_slot{0};
-  void* slots = nullptr;
-  e = cudaGetSymbolAddress(&slots, g_fwd_sched);
-  if (e != cudaSuccess) return e;
-  ForwardArgs args = a;
-  args.sched = static_cast<unsigned*>(slots) + 2 * (next_slot.fetch_add(1u) % kSchedSlots);
-  fwd_kernel<D, kPrecise><<<grid, kFwdThreads, C::kSmemBytes, stream>>>(args);
+  fwd_kernel<D, kPrecise><<<grid, kFwdThreads, C::kSmemBytes, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -6,7 +6,14 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "fa_gb300.h"
+
 namespace fa {
+
+// Wall-clock limit of a kernel's wait on its own pipeline (one second: every such
+// wait is on work the same CTA issued microseconds earlier).  fa_debug_next_wait_limit
+// replaces it for one call.
+constexpr unsigned long long kDefaultWaitNs = 1000000000ull;
 
 struct ForwardArgs {
   CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps over [B*H, Nq or Nk, d] bf16, box {64, 128, 1}, 128B swizzle
@@ -18,9 +25,11 @@ struct ForwardArgs {
   int causal;
   int o_f32;                     // 1: O is fp32, 0: bf16
   int precise;                   // 1: P enters PV as a bf16 hi + lo pair (two MMAs)
-  unsigned* sched;               // set by the launcher: {items claimed, CTAs finished}, zero between launches
+  unsigned* sched;               // work items claimed so far: a counter in the caller's workspace, zeroed
+                                 // on the stream before the launch
   int head_group;                // heads interleaved in the work order (set by the API, see head_group_for)
   unsigned long long* stats;     // optional counters [tiles, skipped, rescales, dq adds]; null: none
+  unsigned long long wait_ns;    // limit of each pipeline wait (kDefaultWaitNs unless a test shortens it)
 };
 
 struct BackwardArgs {
@@ -47,6 +56,7 @@ struct BackwardArgs {
   int o_f32;
   int head_group;                       // heads interleaved in the grid order (set by the API, see head_group_for)
   unsigned long long* stats;            // optional counters [tiles, skipped, rescales, dq adds]; null: none
+  unsigned long long wait_ns;           // limit of each pipeline wait (kDefaultWaitNs unless a test shortens it)
 };
 
 // Heads whose blocks are interleaved in the work order.  Under causality a block's
@@ -102,6 +112,11 @@ cudaError_t launch_forward_keymajor(const KeyMajorArgs& a, cudaStream_t stream);
 cudaError_t read_clear_merge_status(unsigned* out, cudaStream_t stream);
 cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o, float* lse,
                          long long rows, int d, int o_f32, cudaStream_t stream);
+
+// Argument checks of fa_decode, shared with fa_decode_noalloc (fa_api.cu): the
+// workspace the call needs against `workspace_bytes`; no CUDA call.
+fa_status check_decode_args(const void* q, const void* k, const void* v, const float* o, const float* lse, int B,
+                            int H, int L, int d, int n_split, size_t workspace_bytes);
 
 // Split count of the decode path for B*H heads of L keys on `sms` SMs.
 int decode_auto_split(int BH, int L, int sms);

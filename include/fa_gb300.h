@@ -20,7 +20,7 @@
  *  - Errors: argument errors return synchronously (FA_ERR_INVALID_ARG,
  *    FA_ERR_UNSUPPORTED, FA_ERR_WORKSPACE) and queue nothing.  A failed
  *    launch returns FA_ERR_CUDA.  A kernel that hits its internal wait limit
- *    (it never hangs) records FA_ERR_TIMEOUT, read by fa_device_status().
+ *    (it never hangs) records FA_ERR_TIMEOUT, read by fa_get_device_status().
  *  - Supported: d in {64, 128}; N >= 1 (any N: ragged last tiles are masked);
  *    B * H < 2^31, and the forward's B * H * ceil(Nq / 256) work items and the
  *    backward's B * H * ceil(Nk / 128) CTAs below 2^31 as well
@@ -35,17 +35,17 @@
 extern "C" {
 #endif
 
-#define FA_ABI_VERSION 2
+#define FA_ABI_VERSION 3
 
 typedef enum fa_status {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1, /* null pointer, misaligned pointer, bad size */
   FA_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. d not in {64, 128}) */
   FA_ERR_CUDA = 3,        /* a CUDA call or launch failed */
-  FA_ERR_TIMEOUT = 4,     /* a kernel gave up waiting (reported by fa_device_status) */
+  FA_ERR_TIMEOUT = 4,     /* a kernel gave up waiting (reported by fa_get_device_status) */
   FA_ERR_WORKSPACE = 5,   /* workspace missing or smaller than the *_workspace_size() */
   FA_ERR_BOUNDS = 6       /* a kernel of the bounds-checked build (FA_BOUNDS_CHECK) caught an index
-                             outside its buffer and skipped the access (reported by fa_device_status) */
+                             outside its buffer and skipped the access (reported by fa_get_device_status) */
 } fa_status;
 
 typedef enum fa_dtype { FA_BF16 = 0, FA_F32 = 1 } fa_dtype;
@@ -55,6 +55,14 @@ int fa_abi_version(void);
 
 /* Human-readable name of a status code (static string). */
 const char* fa_status_string(fa_status s);
+
+/* Bytes of workspace fa_forward and fa_forward_qk need: the persistent grid's
+ * work counter, padded to 256 bytes.  The size does not depend on the problem
+ * (the arguments are checked only: 0 for B, H, N < 1 or d < 1).  Each call sets
+ * the counter to zero on its stream before its kernel starts, so a workspace
+ * needs no initialisation; it must not be in use by a call whose GPU work
+ * overlaps (two graphs replayed at once need a workspace each). */
+size_t fa_forward_workspace_size(int B, int H, int N, int d, int causal);
 
 /*
  * fa_forward — O = softmax(Q K^T * scale [+ causal mask]) V and LSE.
@@ -71,10 +79,13 @@ const char* fa_status_string(fa_status s);
  *  precise   0: P is rounded to bf16 before the P V product (standard).
  *            1: P enters P V as a bf16 high part plus a bf16 residual (two
  *               tensor-core products), for fp32-grade outputs.
+ *  workspace device scratch of >= fa_forward_workspace_size() bytes, 16-byte
+ *            aligned, owned by the caller (FA_ERR_WORKSPACE if missing or small).
  * Returns FA_OK when the work is queued.
  */
 fa_status fa_forward(const void* q, const void* k, const void* v, void* o, fa_dtype o_dtype, float* lse, int B,
-                     int H, int N, int d, float scale, int causal, int precise, void* stream);
+                     int H, int N, int d, float scale, int causal, int precise, void* workspace,
+                     size_t workspace_bytes, void* stream);
 
 /*
  * fa_forward_qk — fa_forward with Nq queries against Nk keys and a query offset.
@@ -88,12 +99,12 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, fa_dt
  *  q   [B, H, Nq, d] bf16;  k, v  [B, H, Nk, d] bf16.
  *  o   [B, H, Nq, d] in o_dtype, written;  lse  [B, H, Nq] float, written.
  *  Nq, Nk >= 1;  q_start >= 0 (every query then sees key 0) and q_start + Nq
- *  must fit in int: otherwise FA_ERR_INVALID_ARG.  fa_forward(..., N, ...) is
- *  fa_forward_qk(..., Nq = Nk = N, q_start = 0, ...).
+ *  must fit in int: otherwise FA_ERR_INVALID_ARG.  Workspace as for fa_forward.
+ *  fa_forward(..., N, ...) is fa_forward_qk(..., Nq = Nk = N, q_start = 0, ...).
  */
 fa_status fa_forward_qk(const void* q, const void* k, const void* v, void* o, fa_dtype o_dtype, float* lse, int B,
                         int H, int Nq, int Nk, int q_start, int d, float scale, int causal, int precise,
-                        void* stream);
+                        void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of workspace fa_backward needs (pass Nq for fa_backward_qk): 64 per query row over N rounded up to a
  * multiple of 64 (per row, -LSE/scale and -rowsum(dO * O), each as three bf16
@@ -145,8 +156,10 @@ fa_status fa_backward_qk(const void* q, const void* k, const void* v, const void
                          int H, int Nq, int Nk, int q_start, int d, float scale, int causal, void* workspace,
                          size_t workspace_bytes, void* stream);
 
-/* Bytes of workspace fa_decode needs: per-segment states and one arrival
- * counter per (batch, head). */
+/* Bytes of workspace fa_decode needs: per-segment states (B * H * n_split * (d + 2)
+ * floats) and one arrival counter per (batch, head), each part padded to 256
+ * bytes.  0 for an argument < 1, or for a size beyond 2^62 bytes (the counts are
+ * checked before they are multiplied, so the size never wraps around). */
 size_t fa_decode_workspace_size(int B, int H, int d, int n_split);
 
 /*
@@ -166,6 +179,9 @@ size_t fa_decode_workspace_size(int B, int H, int d, int n_split);
  *  workspace  device scratch of >= fa_decode_workspace_size() bytes; the call
  *             clears the counters it holds on `stream` before the kernel runs.
  *  n_split    >= 1 (n_split < 1 is FA_ERR_INVALID_ARG, as the page raises).
+ * B, H > 65535, n_split > 2^30, or a workspace size beyond 2^62 bytes is
+ * FA_ERR_UNSUPPORTED; a workspace smaller than fa_decode_workspace_size() is
+ * FA_ERR_WORKSPACE.
  */
 fa_status fa_decode(const void* q, const void* k, const void* v, float* o, float* lse, int B, int H, int L, int d,
                     float scale, int n_split, float* partials, void* workspace, size_t workspace_bytes,
@@ -216,10 +232,14 @@ fa_status fa_decode_noalloc(const void* q, const void* k, const void* v, float* 
                             int d, float scale, int n_split, float* partials, void* stream);
 
 /*
- * fa_device_status — synchronises `stream`, reads and clears the kernels'
+ * fa_get_device_status — synchronises `stream`, reads and clears the kernels'
  * device status words.  Returns FA_ERR_TIMEOUT if any kernel gave up on a
- * wait since the last call, FA_ERR_CUDA if the CUDA calls fail, else FA_OK.
+ * wait since the last call, FA_ERR_BOUNDS if the bounds-checked build caught
+ * an index outside its buffer, FA_ERR_CUDA if the CUDA calls fail, else FA_OK.
  */
+fa_status fa_get_device_status(void* stream);
+
+/* fa_device_status — the same call as fa_get_device_status (earlier name, kept). */
 fa_status fa_device_status(void* stream);
 
 /* Bytes of workspace fa_forward_keymajor needs: the running O (fp32), maximum and
@@ -303,10 +323,26 @@ fa_status fa_set_stats(unsigned long long* counters);
 /*
  * fa_debug_wait_timeout — test hook for the failure path: queues one CTA that
  * waits on a barrier nothing completes, with a limit of `limit_ns`
- * nanoseconds.  The kernel returns on its own; the next fa_device_status()
+ * nanoseconds.  The kernel returns on its own; the next fa_get_device_status()
  * must report FA_ERR_TIMEOUT.
  */
 fa_status fa_debug_wait_timeout(unsigned long long limit_ns, void* stream);
+
+/*
+ * fa_debug_next_wait_limit — test hook for the failure path of the real kernels:
+ * the next fa_forward, fa_forward_qk, fa_backward or fa_backward_qk call made
+ * from the calling host thread bounds each of its kernels' waits on their own
+ * pipeline by `limit_ns` nanoseconds instead of one second (the deadline is
+ * tested before each sleep, so 0 gives up the first time a wait finds its
+ * barrier phase incomplete).  When a wait gives up, the kernel raises its abort
+ * flag, every role leaves its loop, the copies and products already issued are
+ * waited for (with the normal one-second limit), tensor memory is freed and the
+ * kernel returns; that call's outputs are undefined and the next
+ * fa_get_device_status() reports FA_ERR_TIMEOUT.  The limit is taken by that one
+ * call; a second call of this function before it replaces the pending limit.
+ * More than 5 s is FA_ERR_INVALID_ARG.
+ */
+fa_status fa_debug_next_wait_limit(unsigned long long limit_ns);
 
 #ifdef __cplusplus
 }

@@ -26,7 +26,8 @@ def _declared():
 
 def test_header_declares_the_boundary():
     names = _declared()
-    for required in ("fa_forward", "fa_backward", "fa_decode", "fa_device_status"):
+    for required in ("fa_forward", "fa_forward_workspace_size", "fa_backward", "fa_backward_workspace_size",
+                     "fa_decode", "fa_decode_workspace_size", "fa_get_device_status", "fa_status_string"):
         assert required in names
 
 
@@ -39,7 +40,7 @@ def test_every_declared_symbol_is_exported_and_bound(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.fa_abi_version() == 2
+    assert lib.fa_abi_version() == 3
     assert lib.fa_status_string(0) == b"ok"
     assert lib.fa_status_string(4) == b"device wait timed out"
 
@@ -57,17 +58,49 @@ def test_workspace_sizes(lib):
     partials = 16 * 32 * 64 * 130 * 4
     assert lib.fa_decode_workspace_size(16, 32, 128, 64) == counters + ((partials + 255) // 256) * 256
     assert lib.fa_decode_workspace_size(1, 1, 128, 0) == 0
+    # the forward's workspace holds one work counter, padded to 256 bytes, for any size
+    assert lib.fa_forward_workspace_size(2, 16, 8192, 128, 1) == 256
+    assert lib.fa_forward_workspace_size(1, 1, 1, 64, 0) == 256
+    assert lib.fa_forward_workspace_size(0, 1, 1, 64, 0) == 0
+
+
+def test_decode_workspace_size_never_wraps(lib):
+    # B, H <= 65535 and n_split <= 2^30 would make B * H * n_split * (d + 2) * 4 pass
+    # 2^64: such sizes are reported as 0 (too large), never as a small wrapped value.
+    assert lib.fa_decode_workspace_size(65535, 65535, 128, 1 << 30) == 0
+    r256 = lambda x: ((x + 255) // 256) * 256  # noqa: E731
+    heads = 65535 * 65535
+    assert lib.fa_decode_workspace_size(65535, 65535, 64, 1 << 20) == r256(heads * 4) + r256(heads * (1 << 20) * 264)
+    assert lib.fa_decode_workspace_size(65535, 65535, 128, 1 << 24) == 0  # 2^24 * 520 * heads > 2^62
+    big = lib.fa_decode_workspace_size(65535, 65535, 128, 64)
+    assert big == ((65535 * 65535 * 4 + 255) // 256) * 256 + ((65535 * 65535 * 64 * 130 * 4 + 255) // 256) * 256
 
 
 FAKE = 1 << 20  # a non-null, aligned pointer value; never dereferenced on these paths
 
 
+WS = (FAKE, 256)  # a forward workspace argument pair that passes the checks
+
+
 def test_forward_rejects_bad_arguments(lib):
-    assert lib.fa_forward(None, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 64, 0.0, 0, 0, None) == 1
-    assert lib.fa_forward(FAKE + 2, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 64, 0.0, 0, 0, None) == 1
-    assert lib.fa_forward(FAKE, FAKE, FAKE, FAKE, 7, FAKE, 1, 1, 8, 64, 0.0, 0, 0, None) == 1
-    assert lib.fa_forward(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 0, 64, 0.0, 0, 0, None) == 1
-    assert lib.fa_forward(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 96, 0.0, 0, 0, None) == 2
+    # fa_forward(q, k, v, o, o_dtype, lse, B, H, N, d, scale, causal, precise, workspace, bytes, stream)
+    assert lib.fa_forward(None, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 64, 0.0, 0, 0, *WS, None) == 1
+    assert lib.fa_forward(FAKE + 2, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 64, 0.0, 0, 0, *WS, None) == 1
+    assert lib.fa_forward(FAKE, FAKE, FAKE, FAKE, 7, FAKE, 1, 1, 8, 64, 0.0, 0, 0, *WS, None) == 1
+    assert lib.fa_forward(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 0, 64, 0.0, 0, 0, *WS, None) == 1
+    assert lib.fa_forward(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 96, 0.0, 0, 0, *WS, None) == 2
+    # the workspace: missing, too small, misaligned
+    assert lib.fa_forward(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 64, 0.0, 0, 0, None, 256, None) == 5
+    assert lib.fa_forward(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 64, 0.0, 0, 0, FAKE, 255, None) == 5
+    assert lib.fa_forward(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 64, 0.0, 0, 0, FAKE + 4, 256, None) == 5
+
+
+def test_wait_limit_hook_arguments(lib):
+    # more than 5 s is refused; nothing is launched by these calls.  The last call
+    # sets the normal one-second limit, so no later test inherits a short one.
+    assert lib.fa_debug_next_wait_limit(5_000_000_001) == 1
+    assert lib.fa_debug_next_wait_limit(0) == 0
+    assert lib.fa_debug_next_wait_limit(1_000_000_000) == 0
 
 
 def test_backward_rejects_bad_arguments(lib):
@@ -93,11 +126,12 @@ def test_decode_rejects_bad_arguments(lib):
 
 
 def test_offset_entry_points_reject_bad_arguments(lib):
-    # fa_forward_qk(q, k, v, o, o_dtype, lse, B, H, Nq, Nk, q_start, d, scale, causal, precise, stream)
-    assert lib.fa_forward_qk(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 16, -1, 64, 0.0, 1, 0, None) == 1
-    assert lib.fa_forward_qk(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 0, 0, 64, 0.0, 1, 0, None) == 1
-    assert lib.fa_forward_qk(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 16, 2**31 - 4, 64, 0.0, 1, 0, None) == 1
-    assert lib.fa_forward_qk(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 16, 0, 48, 0.0, 1, 0, None) == 2
+    # fa_forward_qk(q, k, v, o, o_dtype, lse, B, H, Nq, Nk, q_start, d, scale, causal, precise, ws, bytes, stream)
+    assert lib.fa_forward_qk(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 16, -1, 64, 0.0, 1, 0, *WS, None) == 1
+    assert lib.fa_forward_qk(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 0, 0, 64, 0.0, 1, 0, *WS, None) == 1
+    assert lib.fa_forward_qk(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 16, 2**31 - 4, 64, 0.0, 1, 0, *WS, None) == 1
+    assert lib.fa_forward_qk(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 16, 0, 48, 0.0, 1, 0, *WS, None) == 2
+    assert lib.fa_forward_qk(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 16, 0, 64, 0.0, 1, 0, FAKE, 8, None) == 5
     args = [FAKE] * 4 + [0, FAKE, FAKE, FAKE, FAKE, FAKE, 1]
     # fa_backward_qk(..., grad_dtype, B, H, Nq, Nk, q_start, d, scale, causal, workspace, bytes, stream)
     assert lib.fa_backward_qk(*args, 1, 1, 8, 16, -3, 64, 0.0, 1, FAKE, 1 << 20, None) == 1
@@ -108,8 +142,8 @@ def test_offset_entry_points_reject_bad_arguments(lib):
 def test_counts_beyond_32_bits_are_unsupported(lib):
     # B * H = 2^31 heads; then 2^30 heads whose forward items (ceil(1024 / 256) each)
     # or backward CTAs (ceil(1024 / 128) each) pass 2^31: rejected before any CUDA call
-    assert lib.fa_forward(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1 << 16, 1 << 15, 8, 64, 0.0, 0, 0, None) == 2
-    assert lib.fa_forward(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1 << 20, 1 << 10, 1024, 64, 0.0, 0, 0, None) == 2
+    assert lib.fa_forward(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1 << 16, 1 << 15, 8, 64, 0.0, 0, 0, *WS, None) == 2
+    assert lib.fa_forward(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1 << 20, 1 << 10, 1024, 64, 0.0, 0, 0, *WS, None) == 2
     args = [FAKE] * 4 + [0, FAKE, FAKE, FAKE, FAKE, FAKE, 1]
     assert lib.fa_backward(*args, 1 << 20, 1 << 10, 1024, 64, 0.0, 0, FAKE, 1 << 62, None) == 2
 

@@ -83,3 +83,37 @@ def test_reference_arm_line_follows_the_contract(monkeypatch, capsys):
     assert r["cpu_baseline"]["kind"] == "oracle" and r["cpu_baseline"]["value"] == r["value"]
     assert r["cpu_baseline"]["cores"] >= 1 and r["cpu_baseline"]["sample"]
     assert r["e2e"] == {"value": r["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_oracle_parity_leg_reports_errors_against_the_bars():
+    """The bench's oracle leg on tiny samples: outputs equal to the oracle's are within
+    the bars; a perturbed O, LSE or gradient is reported over them."""
+    import numpy as np
+
+    import bench
+    from oracle import attention_dense, attention_dense_backward, attention_split_decode
+
+    rng = np.random.default_rng(0)
+    q, k, v, do = (rng.standard_normal((40, 64)) for _ in range(4))
+    o, lse = attention_dense(q, k, v, causal=True)
+    grads = attention_dense_backward(q, k, v, do, causal=True)
+    qd, kd, vd = rng.standard_normal((3, 1, 64)), rng.standard_normal((3, 50, 64)), rng.standard_normal((3, 50, 64))
+    od, ld, _ = attention_split_decode(qd, kd, vd, 4)
+
+    def samples(do_shift=0.0, lse_shift=0.0, dk_scale=1.0):
+        return {
+            "fb": {"kind": "attention", "causal": True, "o_dtype": "bf16", "subset": "tiny",
+                   "inputs": {"q": q, "k": k, "v": v, "do": do},
+                   "gpu": {"o": o + do_shift, "lse": lse + lse_shift, "dq": grads[0], "dk": grads[1] * dk_scale,
+                           "dv": grads[2]}},
+            "dec": {"kind": "decode", "n_split": 4, "o_dtype": "f32", "subset": "tiny",
+                    "inputs": {"q": qd, "k": kd, "v": vd}, "gpu": {"o": od, "lse": ld[..., 0]}},
+        }
+
+    ok = bench.oracle_parity(samples())
+    assert ok["fb"]["within_bars"] and ok["dec"]["within_bars"]
+    assert ok["fb"]["o_max_abs"] < 1e-12 and ok["fb"]["dk_rel_fro"] < 1e-12
+    assert not bench.oracle_parity(samples(do_shift=0.05))["fb"]["within_bars"]
+    assert not bench.oracle_parity(samples(lse_shift=3e-3))["fb"]["within_bars"]
+    bad = bench.oracle_parity(samples(dk_scale=1.05))["fb"]
+    assert not bad["within_bars"] and abs(bad["dk_rel_fro"] - 0.05) < 1e-9

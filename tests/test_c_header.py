@@ -38,9 +38,12 @@ int main(void) {
   CHECK(fa_decode_workspace_size(16, 32, 128, 64) > 0);
   CHECK(fa_decode_auto_split(0, 32, 32768) == 0);
   /* argument errors */
-  CHECK(fa_forward(NULL, p, p, p, FA_BF16, f, 1, 1, 8, 64, 0.f, 0, 0, NULL) == FA_ERR_INVALID_ARG);
-  CHECK(fa_forward(p, p, p, p, FA_BF16, f, 1, 1, 8, 96, 0.f, 0, 0, NULL) == FA_ERR_UNSUPPORTED);
-  CHECK(fa_forward_qk(p, p, p, p, FA_BF16, f, 1, 1, 8, 16, -1, 64, 0.f, 1, 0, NULL) == FA_ERR_INVALID_ARG);
+  CHECK(fa_forward_workspace_size(2, 16, 8192, 128, 1) == 256);
+  CHECK(fa_forward(NULL, p, p, p, FA_BF16, f, 1, 1, 8, 64, 0.f, 0, 0, p, 256, NULL) == FA_ERR_INVALID_ARG);
+  CHECK(fa_forward(p, p, p, p, FA_BF16, f, 1, 1, 8, 96, 0.f, 0, 0, p, 256, NULL) == FA_ERR_UNSUPPORTED);
+  CHECK(fa_forward(p, p, p, p, FA_BF16, f, 1, 1, 8, 64, 0.f, 0, 0, ws_small, sizeof ws_small, NULL) ==
+        FA_ERR_WORKSPACE);
+  CHECK(fa_forward_qk(p, p, p, p, FA_BF16, f, 1, 1, 8, 16, -1, 64, 0.f, 1, 0, p, 256, NULL) == FA_ERR_INVALID_ARG);
   CHECK(fa_backward(p, p, p, p, FA_BF16, f, p, p, p, p, (fa_dtype)7, 1, 1, 8, 64, 0.f, 1, p, 1u << 20, NULL) ==
         FA_ERR_INVALID_ARG);
   CHECK(fa_backward(p, p, p, p, FA_BF16, f, p, p, p, p, FA_BF16, 1, 1, 8, 64, 0.f, 1, ws_small, sizeof ws_small,

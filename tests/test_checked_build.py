@@ -24,7 +24,7 @@ for name in {names!r}:
     assert hasattr(lib, name), name
 assert lib.fa_status_string(6) == b"index outside its buffer (bounds-checked build)"
 assert lib.fa_backward_workspace_size(2, 16, 8192, 128, 1) == 2 * 16 * 8192 * 64
-assert lib.fa_forward(None, 64, 64, 64, 0, 64, 1, 1, 8, 64, 0.0, 0, 0, None) == 1
+assert lib.fa_forward(None, 64, 64, 64, 0, 64, 1, 1, 8, 64, 0.0, 0, 0, 64, 256, None) == 1
 print("ok")
 """
 

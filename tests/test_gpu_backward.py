@@ -83,10 +83,11 @@ def test_backward_causal_b4h16_n2048_d64_full():
 
 
 def test_backward_causal_b2h16_n8192_d128_qk8_sampled_heads():
-    """Full-size causal backward with Q, K x8 (seed 2): two whole heads compared
-    element by element; the dK / dV invariants on every head."""
+    """Full-size causal backward with Q, K x8 (seed 2): four whole heads compared
+    element by element (both batches, first, middle and last heads); the dK / dV
+    invariants on every head."""
     q, k, v, do, dq, dk, dv = _run(2, 16, 8192, 128, True, seed=2, mult=8.0)
-    for b, h in [(0, 3), (1, 12)]:
+    for b, h in [(0, 0), (0, 10), (1, 6), (1, 15)]:
         ref = attention_dense_backward(f64(q[b, h]), f64(k[b, h]), f64(v[b, h]), f64(do[b, h]), causal=True)
         _check((dq[b, h], dk[b, h], dv[b, h]), ref)
     _invariants(dk, dv, do)

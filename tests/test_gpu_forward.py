@@ -91,10 +91,11 @@ def test_forward_causal_b4h16_n2048_d64_full(out):
 
 @pytest.mark.parametrize("out", ["bf16", "f32"])
 def test_forward_causal_b2h16_n8192_d128_qk8_sampled(out):
-    """Full-size causal forward with Q, K x8 (seed 2): two whole heads compared
-    element by element, plus sampled rows of every head."""
+    """Full-size causal forward with Q, K x8 (seed 2): four whole heads compared
+    element by element (both batches, first, middle and last heads), plus sampled
+    rows of every head."""
     q, k, v, o, lse = _run(2, 16, 8192, 128, True, seed=2, out=out, mult=8.0)
-    for b, h in [(0, 0), (1, 15)]:
+    for b, h in [(0, 0), (0, 9), (1, 4), (1, 15)]:
         ref_o, ref_l = attention_dense(f64(q[b, h]), f64(k[b, h]), f64(v[b, h]), causal=True)
         _check(o[b, h], lse[b, h], ref_o, ref_l, out)
     rows = [0, 1, 127, 128, 4095, 8190, 8191]
@@ -106,10 +107,12 @@ def test_forward_causal_b2h16_n8192_d128_qk8_sampled(out):
 
 @pytest.mark.parametrize("out", ["bf16", "f32"])
 def test_forward_b1h32_n16384_d128_sampled(out):
-    """Full-size non-causal forward (seed 3): one whole head plus sampled rows of every head."""
+    """Full-size non-causal forward (seed 3): four whole heads compared element by
+    element, plus sampled rows of every head."""
     q, k, v, o, lse = _run(1, 32, 16384, 128, False, seed=3, out=out)
-    ref_o, ref_l = attention_dense(f64(q[0, 5]), f64(k[0, 5]), f64(v[0, 5]))
-    _check(o[0, 5], lse[0, 5], ref_o, ref_l, out)
+    for h in (0, 5, 17, 31):
+        ref_o, ref_l = attention_dense(f64(q[0, h]), f64(k[0, h]), f64(v[0, h]))
+        _check(o[0, h], lse[0, h], ref_o, ref_l, out)
     rows = [0, 255, 256, 9000, 16383]
     for h in range(32):
         ref_o, ref_l = attention_dense_rows(f64(q[0, h]), f64(k[0, h]), f64(v[0, h]), rows)

@@ -94,3 +94,54 @@ def test_forward_backward_decode_captured_and_replayed():
                 for gname, gg, rr in zip(("dQ", "dK", "dV"), (t[b, h] for t in got[2:5]), r):
                     assert rel_fro(f64(gg), rr) <= GRAD_REL_FRO, gname
 
+
+
+def test_two_captured_forwards_replayed_concurrently_on_two_streams():
+    """Two forwards captured into two graphs, each with its own workspace (the
+    persistent grid's work counter) and outputs, replayed at the same time on two
+    streams. The small problem's grid takes a few SMs while the large one's fills
+    the rest, so the two grids run side by side and claim work items at the same
+    time. Each result must equal an eager call on the same inputs bit for bit: no
+    item is lost or computed twice."""
+    from exact_attention_flash_gb300 import fa_forward, fa_get_device_status, forward_workspace_bytes
+    from exact_attention_flash_gb300.workloads import make_attention_inputs
+
+    shapes = [(2, 16, 4096, 128, True), (1, 4, 2048, 64, False)]
+    runs = []
+    for i, (B, H, N, d, causal) in enumerate(shapes):
+        q, k, v, _ = make_attention_inputs(B, H, N, d, 400 + i, "cuda", with_do=False)
+        ref_o, ref_l = fa_forward(q, k, v, causal=causal)
+        o = torch.empty_like(ref_o)
+        lse = torch.empty_like(ref_l)
+        ws = torch.empty(forward_workspace_bytes(B, H, N, d, causal), device="cuda", dtype=torch.uint8)
+        runs.append(dict(q=q, k=k, v=v, causal=causal, o=o, lse=lse, ws=ws, ref=(ref_o, ref_l)))
+    torch.cuda.synchronize()
+
+    streams = [torch.cuda.Stream() for _ in runs]
+    graphs = []
+    for r, s in zip(runs, streams):
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):  # warm-up outside the capture
+            fa_forward(r["q"], r["k"], r["v"], causal=r["causal"], out=r["o"], lse=r["lse"], workspace=r["ws"])
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fa_forward(r["q"], r["k"], r["v"], causal=r["causal"], out=r["o"], lse=r["lse"], workspace=r["ws"])
+        graphs.append(g)
+    torch.cuda.synchronize()
+
+    for trial in range(20):
+        for r in runs:
+            r["o"].fill_(float("nan"))
+            r["lse"].fill_(float("nan"))
+        torch.cuda.synchronize()
+        order = [1, 0] if trial % 2 == 0 else [0, 1]
+        for i in order:
+            with torch.cuda.stream(streams[i]):
+                graphs[i].replay()
+        torch.cuda.synchronize()
+        assert fa_get_device_status() == 0
+        for i, r in enumerate(runs):
+            assert torch.equal(r["o"], r["ref"][0]), (trial, i, "O")
+            assert torch.equal(r["lse"], r["ref"][1]), (trial, i, "LSE")
