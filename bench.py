@@ -441,7 +441,7 @@ def workload_records(peaks, reps, dev, stream, keep_samples):
                 samples[name] = {"kind": "decode", "n_split": w.n_split, "o_dtype": "f32",
                                  "subset": f"{len(heads)} of {w.B * w.H} heads",
                                  "inputs": {"q": pick(q), "k": pick(k), "v": pick(v)},
-                                 "gpu": {"o": pick(o), "lse": _f64(torch.stack([lse[b, h:h + 1] for b, h in heads]))}}
+                                 "gpu": {"o": pick(o), "lse": _f64(torch.stack([lse[b, h] for b, h in heads]))}}
             del q, k, v, ws, o, lse
         else:
             q, k, v, do = make_inputs(w, dev)

@@ -53,7 +53,7 @@ SIGNATURES = {
     "fa_forward_keymajor": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
     "fa_decode_auto_split": (_I, [_I, _I, _I]),
     "fa_debug_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
-    "fa_debug_next_wait_limit": (_I, [ctypes.c_ulonglong]),
+    "fa_debug_abort_next_call": (_I, []),
 }
 
 _lib = None

@@ -97,15 +97,14 @@ size_t backward_bias_bytes(int B, int H, int N) {
 // Counters set by fa_set_stats for the calling host thread's calls (null: none).
 thread_local unsigned long long* t_stats = nullptr;
 
-// Wait limit for the calling host thread's next forward or backward call, set by
-// fa_debug_next_wait_limit; taken (and cleared) by that one call.
-thread_local bool t_next_wait_set = false;
-thread_local unsigned long long t_next_wait_ns = 0;
+// Set by fa_debug_abort_next_call: the calling host thread's next forward or
+// backward call aborts on purpose; taken (and cleared) by that one call.
+thread_local bool t_abort_next = false;
 
-unsigned long long take_wait_limit() {
-  const unsigned long long ns = t_next_wait_set ? t_next_wait_ns : fa::kDefaultWaitNs;
-  t_next_wait_set = false;
-  return ns;
+int take_debug_abort() {
+  const bool v = t_abort_next;
+  t_abort_next = false;
+  return v ? 1 : 0;
 }
 
 // The forward's workspace: one 32-bit work counter, padded.
@@ -194,7 +193,7 @@ fa_status fa_forward_qk(const void* q, const void* k, const void* v, void* o, fa
   a.o_f32 = (o_dtype == FA_F32) ? 1 : 0;
   a.precise = precise ? 1 : 0;
   a.stats = t_stats;
-  a.wait_ns = take_wait_limit();
+  a.debug_abort = take_debug_abort();
   // The persistent grid claims its work items from this counter: zero it first,
   // in stream order, so that the workspace needs no initialisation by the caller.
   a.sched = static_cast<unsigned*>(workspace);
@@ -271,7 +270,7 @@ fa_status fa_backward_qk(const void* q, const void* k, const void* v, const void
   a.head_group = fa::head_group_for(a.causal, 2ll * Nq * d * 2 + static_cast<long long>(Nq) * d * 4, B * H);  // Q, dO, dQ
   a.o_f32 = (o_dtype == FA_F32) ? 1 : 0;
   a.stats = t_stats;
-  a.wait_ns = take_wait_limit();
+  a.debug_abort = take_debug_abort();
   const cudaError_t e = fa::launch_backward(a, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return FA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -406,10 +405,8 @@ fa_status fa_set_stats(unsigned long long* counters) {
 
 fa_status fa_device_status(void* stream) { return fa_get_device_status(stream); }
 
-fa_status fa_debug_next_wait_limit(unsigned long long limit_ns) {
-  if (limit_ns > 5000000000ull) return FA_ERR_INVALID_ARG;
-  t_next_wait_ns = limit_ns;
-  t_next_wait_set = true;
+fa_status fa_debug_abort_next_call(void) {
+  t_abort_next = true;
   return FA_OK;
 }
 

@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         int issued = 0;
         for (int n = 0; n < n_steps; ++n) {
           const int s = n % C::kStages;
-          if (n >= C::kStages && !mbar_wait(&sh.q_empty[s], ((n / C::kStages) - 1) & 1, &sh.abort, &g_bwd_status, a.wait_ns))
+          if (n >= C::kStages && !mbar_wait(&sh.q_empty[s], ((n / C::kStages) - 1) & 1, &sh.abort, &g_bwd_status))
             break;
           const int q0 = (i_start + n) * kBQ;
           // The query block's bias tiles from the workspace (4 KB aligned): block blk of
@@ -350,24 +350,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       // ------------------------------------------------------------ the issuer's waits
       // The same sequence of rendezvous as the MMA issuer, each after the wait that
       // the product issued next depends on.
-      bool ok = warp_wait(&sh.kv_full, 0, &sh.abort, &g_bwd_status, a.wait_ns) &&
-                warp_wait(&sh.q_full[0], 0, &sh.abort, &g_bwd_status, a.wait_ns);
+      bool ok = warp_wait(&sh.kv_full, 0, &sh.abort, &g_bwd_status) &&
+                warp_wait(&sh.q_full[0], 0, &sh.abort, &g_bwd_status);
+      if (a.debug_abort) {  // failure-path test: act as if this wait had timed out
+        if (lane == 0) raise_abort(&sh.abort, &g_bwd_status);
+        ok = false;
+      }
       ok = issuer_rendezvous(ok);
       for (int n = 0; ok && n < n_steps; ++n) {
         const int b = n & 1;
         const bool next = n + 1 < n_steps;
         if (next) {
           const int s1 = (n + 1) % C::kStages;
-          if (!(ok = issuer_rendezvous(warp_wait(&sh.q_full[s1], ((n + 1) / C::kStages) & 1, &sh.abort, &g_bwd_status, a.wait_ns))))
+          if (!(ok = issuer_rendezvous(warp_wait(&sh.q_full[s1], ((n + 1) / C::kStages) & 1, &sh.abort, &g_bwd_status))))
             break;
         }
-        if (!(ok = issuer_rendezvous(warp_wait(&sh.p_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status, a.wait_ns)))) break;
+        if (!(ok = issuer_rendezvous(warp_wait(&sh.p_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status)))) break;
         if (next) {
           // dP^T(n+1) overwrites dQ^T(n-1)
-          const bool w = n < 1 || warp_wait(&sh.dq_empty[(n - 1) & 1], ((n - 1) >> 1) & 1, &sh.abort, &g_bwd_status, a.wait_ns);
+          const bool w = n < 1 || warp_wait(&sh.dq_empty[(n - 1) & 1], ((n - 1) >> 1) & 1, &sh.abort, &g_bwd_status);
           if (!(ok = issuer_rendezvous(w))) break;
         }
-        if (!(ok = issuer_rendezvous(warp_wait(&sh.ds_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status, a.wait_ns)))) break;
+        if (!(ok = issuer_rendezvous(warp_wait(&sh.ds_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status)))) break;
       }
     }
   } else if (warp < kWriterWarp0) {
@@ -386,11 +390,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       const int q0 = (i_start + n) * kBQ;
       // The dS tile of step n - 2 must have been read by dQ^T(n - 2) (checked first:
       // it is long done, and the check's latency hides behind the wait for S^T).
-      if (n >= 2 && !__all_sync(0xffffffffu, mbar_wait(&sh.ds_empty[b], ((n >> 1) - 1) & 1, &sh.abort, &g_bwd_status, a.wait_ns))) {
+      if (n >= 2 && !__all_sync(0xffffffffu, mbar_wait(&sh.ds_empty[b], ((n >> 1) - 1) & 1, &sh.abort, &g_bwd_status))) {
         ok = false;
         break;
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(&sh.s_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status, a.wait_ns))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sh.s_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status))) {
         ok = false;
         break;
       }
@@ -424,7 +428,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       tmem_st16(s_tm, pk);
       tc_fence_before();
       mbar_arrive_warp(&sh.p_full[b]);
-      if (!__all_sync(0xffffffffu, mbar_wait(&sh.dp_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status, a.wait_ns))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sh.dp_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status))) {
         ok = false;
         break;
       }
@@ -464,7 +468,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     constexpr int kBoxBytes = kBKV * 128;  // 16 KB
     const int box_cols = a.grad_bf16 ? 64 : 32;  // features per box
     const int n_boxes = D / box_cols;            // per tensor
-    const bool e_ok = ok && __all_sync(0xffffffffu, mbar_wait(&sh.dkdv_full, 0, &sh.abort, &g_bwd_status, a.wait_ns));
+    const bool e_ok = ok && __all_sync(0xffffffffu, mbar_wait(&sh.dkdv_full, 0, &sh.abort, &g_bwd_status));
     if (e_ok) {
       tc_fence_after();
       uint8_t* stage_v = sQ;                        // boxes of dV, then of dK
@@ -528,7 +532,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     for (int n = 0; n < n_steps; ++n) {
       const int b = n & 1;
       const int q0 = (i_start + n) * kBQ + 32 * half;
-      if (!__all_sync(0xffffffffu, mbar_wait(&sh.dq_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status, a.wait_ns))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&sh.dq_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status))) break;
       uint32_t v[32];
       tc_fence_after();
       if (has_rows) tmem_ld32(tmem_addr(tmem, lane_base, 128 + b * kBQ + 32 * half), v);

@@ -23,6 +23,10 @@
 //               row of O in TMEM when the running max grows by more than a factor 2^32
 //               (the final O / l uses the same reference max, so this is exact).
 // Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 and O_1 after.
+// With d = 64 the last 128 columns hold P_0 and P_1 (64 each, bf16 pairs), so the
+// issuer starts S_t of the next key tile as soon as the softmax has loaded S_t into
+// registers; with d = 128, P overwrites the first half of S_t and the next S_t waits
+// for the P V product that reads it.
 // Work is done in base 2: x = S * scale * log2(e), p = 2^(x - m).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -37,7 +41,6 @@ namespace fa {
 namespace {
 
 __device__ unsigned g_fwd_status;
-static_assert(kWaitLimitNs == kDefaultWaitNs, "drain waits keep the default pipeline limit");
 
 constexpr int kBM = 128;             // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;             // keys per KV tile
@@ -67,6 +70,11 @@ struct FwdCfg {
   static constexpr int kTileBytes = kBM * D * 2;        // one 128-row bf16 tile
   static constexpr int kStages = (D == 128) ? 2 : 4;
   static constexpr int kOCol = 256;                     // O_0 column; O_1 at kOCol + D
+  // With d = 64 two tiles' S (2 x 128 columns) and O (2 x 64) leave 128 columns of
+  // tensor memory free: P gets its own 64 columns per tile there, so the next S
+  // product can overwrite S as soon as the softmax has loaded it (see kSPrefetch).
+  static constexpr int kPCol = kOCol + kTiles * D;      // P_0 column; P_1 at kPCol + kBN / 2
+  static_assert(D != 64 || kPCol + kTiles * kBN / 2 <= 512, "S, O and P fit the 512 columns at d = 64");
   static constexpr int kSmemBytes = kTiles * kTileBytes + kStages * 2 * kTileBytes + 1024;
 };
 
@@ -79,6 +87,7 @@ struct FwdBarriers {
   uint64_t q_full[kTiles], q_empty[kTiles];
   uint64_t k_full[4], v_full[4], kv_empty[4];
   uint64_t s_full[kTiles], p_half[kTiles], p_full[kTiles], o_full[kTiles], o_empty[kTiles];
+  uint64_t s_free[kTiles], pv_done[kTiles];  // S-prefetch schedule only (d = 64)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -120,6 +129,13 @@ __device__ __forceinline__ FwdItem fwd_item(const ForwardArgs& a, int item) {
 template <int D, bool kPrecise>
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ ForwardArgs a) {
   using C = FwdCfg<D>;
+  // S prefetch (d = 64, standard precision): P_t lives in its own tensor-memory
+  // columns, so S_t(j + 1) is issued as soon as the softmax has loaded S_t(j)
+  // (s_free) instead of after P_t V(j) has read P from the S columns.  Each tile's
+  // softmax then runs step after step without waiting for the tensor core; the
+  // softmax waits for P_t V(j - 1) (pv_done) only before it overwrites P_t or
+  // rescales O_t.  With d = 128 the columns are not there (S 2 x 128 + O 2 x 128).
+  constexpr bool kSPrefetch = (D == 64) && !kPrecise;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                                   // [kTiles][kTileBytes]
@@ -157,6 +173,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       mbar_init(&bars.p_half[t], kBM / 32);  // one arrival per softmax warp of the tile
       mbar_init(&bars.p_full[t], kBM / 32);
       mbar_init(&bars.o_full[t], 1);
+      mbar_init(&bars.s_free[t], kBM / 32);
+      mbar_init(&bars.pv_done[t], 1);
     }
     mbar_init(&bars.drain, 1);
     fence_barrier_init();
@@ -184,7 +202,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           // Claim the next item and publish it (n_items once none is left).
           const int r = it % kItemRing;
           if (it >= kItemRing &&
-              !mbar_wait(&bars.item_empty[r], ((it / kItemRing) - 1) & 1, &bars.abort, &g_fwd_status, a.wait_ns))
+              !mbar_wait(&bars.item_empty[r], ((it / kItemRing) - 1) & 1, &bars.abort, &g_fwd_status))
             break;
           const unsigned claimed = atomicAdd(a.sched, 1u);
           const int item = claimed < static_cast<unsigned>(n_items) ? static_cast<int>(claimed) : n_items;
@@ -194,7 +212,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           const FwdItem w = fwd_item(a, item);
           // Q tile t is reloaded once the previous item's last S_t product has read it.
           for (int t = 0; ok && t < kTiles; ++t) {
-            if (it > 0 && !mbar_wait(&bars.q_empty[t], (it - 1) & 1, &bars.abort, &g_fwd_status, a.wait_ns)) {
+            if (it > 0 && !mbar_wait(&bars.q_empty[t], (it - 1) & 1, &bars.abort, &g_fwd_status)) {
               ok = false;
               break;
             }
@@ -206,7 +224,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           }
           for (int j = 0; ok && j < w.n_kv[kTiles - 1]; ++j) {
             const int s = g % C::kStages;
-            if (g >= C::kStages && !mbar_wait(&bars.kv_empty[s], ((g / C::kStages) - 1) & 1, &bars.abort, &g_fwd_status, a.wait_ns)) {
+            if (g >= C::kStages && !mbar_wait(&bars.kv_empty[s], ((g / C::kStages) - 1) & 1, &bars.abort, &g_fwd_status)) {
               ok = false;
               break;
             }
@@ -258,14 +276,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         // first: the item's first key tile (O is written, not accumulated).
         auto issue_pv = [&](int t, int s, int step, bool first) -> bool {
           const uint64_t v_d = desc_add(dV, s * C::kTileBytes);
-          const uint32_t o_tm = tmem + C::kOCol + t * D, p_tm = tmem + t * kBN;
+          const uint32_t o_tm = tmem + C::kOCol + t * D;
+          const uint32_t p_tm = kSPrefetch ? tmem + C::kPCol + t * (kBN / 2) : tmem + t * kBN;
           const uint32_t acc0 = first ? 0u : 1u;
-          if (!warp_wait(&bars.p_half[t], step & 1, &bars.abort, &g_fwd_status, a.wait_ns)) return false;
+          if (!warp_wait(&bars.p_half[t], step & 1, &bars.abort, &g_fwd_status)) return false;
           tc_fence_after();
   #pragma unroll
           for (int kk = 0; kk < kBN / 32; ++kk)
             umma_ts(o_tm, p_tm + kk * 8, desc_add(v_d, kk * 16 * 128), kIdO, kk > 0 ? 1u : acc0, leader);
-          if (!warp_wait(&bars.p_full[t], step & 1, &bars.abort, &g_fwd_status, a.wait_ns)) return false;
+          if (!warp_wait(&bars.p_full[t], step & 1, &bars.abort, &g_fwd_status)) return false;
           tc_fence_after();
   #pragma unroll
           for (int kk = kBN / 32; kk < kBN / 16; ++kk)
@@ -286,7 +305,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         bool ok = true;
         for (int it = 0; ok; ++it) {
           const int r = it % kItemRing;
-          if (!warp_wait(&bars.item_full[r], (it / kItemRing) & 1, &bars.abort, &g_fwd_status, a.wait_ns)) break;
+          if (!warp_wait(&bars.item_full[r], (it / kItemRing) & 1, &bars.abort, &g_fwd_status)) break;
           const int item = bars.item[r];
           mbar_arrive_warp(&bars.item_empty[r]);
           if (item >= n_items) break;
@@ -298,45 +317,99 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
               n_skipped += n_kv_total - w.n_kv[t];
             }
           const int s0 = g % C::kStages;
-          ok = warp_wait(&bars.k_full[s0], (g / C::kStages) & 1, &bars.abort, &g_fwd_status, a.wait_ns);
-          for (int t = 0; ok && t < kTiles; ++t) {
-            if (!warp_wait(&bars.q_full[t], it & 1, &bars.abort, &g_fwd_status, a.wait_ns)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_s(t, s0);
-          }
-          for (int j = 0; ok && j < w.n_kv[kTiles - 1]; ++j, ++g) {
-            const int s = g % C::kStages, sn = (g + 1) % C::kStages;
-            const uint32_t phn = ((g + 1) / C::kStages) & 1;
-            if (!warp_wait(&bars.v_full[s], (g / C::kStages) & 1, &bars.abort, &g_fwd_status, a.wait_ns)) {
-              ok = false;
-              break;
-            }
-            for (int t = 0; t < kTiles; ++t) {
-              if (j >= w.n_kv[t]) continue;  // tile 0 may need one key tile fewer
-              // The item's first P V_t overwrites O_t: the previous item's epilogue must
-              // have read O_t out of tensor memory.
-              if (j == 0 && it > 0 && !warp_wait(&bars.o_empty[t], (it - 1) & 1, &bars.abort, &g_fwd_status, a.wait_ns)) {
+          ok = warp_wait(&bars.k_full[s0], (g / C::kStages) & 1, &bars.abort, &g_fwd_status);
+          if constexpr (kSPrefetch) {
+            // The item's first S_t: Q_t reloaded, and S_t of the previous item's last
+            // step loaded by the softmax.
+            for (int t = 0; ok && t < kTiles; ++t) {
+              if (!warp_wait(&bars.q_full[t], it & 1, &bars.abort, &g_fwd_status) ||
+                  (step[t] > 0 &&
+                   !warp_wait(&bars.s_free[t], (step[t] - 1) & 1, &bars.abort, &g_fwd_status))) {
                 ok = false;
                 break;
               }
-              if (!issue_pv(t, s, step[t] + j, j == 0)) {
-                ok = false;
-                break;
-              }
-              if (t == kTiles - 1) umma_commit(&bars.kv_empty[s], leader);
-              if (j + 1 < w.n_kv[t]) {
-                if (!warp_wait(&bars.k_full[sn], phn, &bars.abort, &g_fwd_status, a.wait_ns)) {
+              tc_fence_after();
+              issue_s(t, s0);
+              if (w.n_kv[t] == 1) umma_commit(&bars.q_empty[t], leader);  // its only S_t has read Q_t
+            }
+            for (int j = 0; ok && j < w.n_kv[kTiles - 1]; ++j, ++g) {
+              const int s = g % C::kStages, sn = (g + 1) % C::kStages;
+              const uint32_t phn = ((g + 1) / C::kStages) & 1;
+              // S_t(j + 1) once the softmax has loaded S_t(j) and K(j + 1) has landed.
+              for (int t = 0; t < kTiles; ++t) {
+                if (j + 1 >= w.n_kv[t]) continue;
+                if (!warp_wait(&bars.k_full[sn], phn, &bars.abort, &g_fwd_status) ||
+                    !warp_wait(&bars.s_free[t], (step[t] + j) & 1, &bars.abort, &g_fwd_status)) {
                   ok = false;
                   break;
                 }
                 tc_fence_after();
                 issue_s(t, sn);
-              } else {
-                umma_commit(&bars.o_full[t], leader);   // O_t of this item is complete
-                umma_commit(&bars.q_empty[t], leader);  // its last S_t product has read Q_t
+                if (j + 2 == w.n_kv[t]) umma_commit(&bars.q_empty[t], leader);  // the item's last S_t
+              }
+              if (!ok ||
+                  !warp_wait(&bars.v_full[s], (g / C::kStages) & 1, &bars.abort, &g_fwd_status)) {
+                ok = false;
+                break;
+              }
+              // O_t += P_t(j) V(j) once the softmax has written P_t(j).
+              for (int t = 0; t < kTiles; ++t) {
+                if (j >= w.n_kv[t]) continue;  // tile 0 may need one key tile fewer
+                if (j == 0 && it > 0 &&
+                    !warp_wait(&bars.o_empty[t], (it - 1) & 1, &bars.abort, &g_fwd_status)) {
+                  ok = false;
+                  break;
+                }
+                if (!issue_pv(t, s, step[t] + j, j == 0)) {
+                  ok = false;
+                  break;
+                }
+                umma_commit(&bars.pv_done[t], leader);
+                if (j + 1 == w.n_kv[t]) umma_commit(&bars.o_full[t], leader);  // O_t of this item is complete
+              }
+              if (!ok) break;
+              umma_commit(&bars.kv_empty[s], leader);
+            }
+          } else {
+            for (int t = 0; ok && t < kTiles; ++t) {
+              if (!warp_wait(&bars.q_full[t], it & 1, &bars.abort, &g_fwd_status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_s(t, s0);
+            }
+            for (int j = 0; ok && j < w.n_kv[kTiles - 1]; ++j, ++g) {
+              const int s = g % C::kStages, sn = (g + 1) % C::kStages;
+              const uint32_t phn = ((g + 1) / C::kStages) & 1;
+              if (!warp_wait(&bars.v_full[s], (g / C::kStages) & 1, &bars.abort, &g_fwd_status)) {
+                ok = false;
+                break;
+              }
+              for (int t = 0; t < kTiles; ++t) {
+                if (j >= w.n_kv[t]) continue;  // tile 0 may need one key tile fewer
+                // The item's first P V_t overwrites O_t: the previous item's epilogue must
+                // have read O_t out of tensor memory.
+                if (j == 0 && it > 0 && !warp_wait(&bars.o_empty[t], (it - 1) & 1, &bars.abort, &g_fwd_status)) {
+                  ok = false;
+                  break;
+                }
+                if (!issue_pv(t, s, step[t] + j, j == 0)) {
+                  ok = false;
+                  break;
+                }
+                if (t == kTiles - 1) umma_commit(&bars.kv_empty[s], leader);
+                if (j + 1 < w.n_kv[t]) {
+                  if (!warp_wait(&bars.k_full[sn], phn, &bars.abort, &g_fwd_status)) {
+                    ok = false;
+                    break;
+                  }
+                  tc_fence_after();
+                  issue_s(t, sn);
+                } else {
+                  umma_commit(&bars.o_full[t], leader);   // O_t of this item is complete
+                  umma_commit(&bars.q_empty[t], leader);  // its last S_t product has read Q_t
+                }
               }
             }
           }
@@ -360,13 +433,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     const int lane_base = (warp & 3) * 32;    // TMEM lane quarter of this warp
     const uint32_t s_tm = tmem_addr(tmem, lane_base, t * kBN);
     const uint32_t o_tm = tmem_addr(tmem, lane_base, C::kOCol + t * D);
+    // P_t: over the first 64 columns of S_t, or in its own columns with S prefetch.
+    const uint32_t p_tm = kSPrefetch ? tmem_addr(tmem, lane_base, C::kPCol + t * (kBN / 2)) : s_tm;
     const float sl2 = a.scale_log2;
     int step = 0;  // this tile's steps across items (the S and P barriers' phase)
     unsigned n_rescales = 0;  // running-max growths of this row (fa_set_stats counters)
     bool ok = true;
+    if (a.debug_abort) {  // failure-path test: act as if the first wait had timed out
+      if (lane == 0) raise_abort(&bars.abort, &g_fwd_status);
+      ok = false;  // nothing is handed over, so the other roles' next waits give up too
+    }
     for (int it = 0; ok; ++it) {
     const int ring = it % kItemRing;
-    if (!__all_sync(0xffffffffu, mbar_wait(&bars.item_full[ring], (it / kItemRing) & 1, &bars.abort, &g_fwd_status, a.wait_ns)))
+    if (!__all_sync(0xffffffffu, mbar_wait(&bars.item_full[ring], (it / kItemRing) & 1, &bars.abort, &g_fwd_status)))
       break;
     const int item = bars.item[ring];
     mbar_arrive_warp(&bars.item_empty[ring]);
@@ -380,7 +459,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     float l_hat = 0.f;  // sum of the bf16-rounded p that enter P V: the normaliser of O
     for (int j = 0; j < w.n_kv[t]; ++j, ++step) {
       // Lanes leave together: the TMEM accesses below are warp-collective.
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars.s_full[t], step & 1, &bars.abort, &g_fwd_status, a.wait_ns))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars.s_full[t], step & 1, &bars.abort, &g_fwd_status))) {
         ok = false;
         break;
       }
@@ -394,6 +473,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         tmem_ld64(s_tm + 64, u);
 #pragma unroll
         for (int i = 0; i < 64; ++i) x[64 + i] = __uint_as_float(u[i]);
+      }
+      if constexpr (kSPrefetch) {  // S_t is in registers: the next S_t product may overwrite it
+        tc_fence_before();
+        mbar_arrive_warp(&bars.s_free[t]);
       }
       const int key0 = j * kBN;
       const bool need_mask = (key0 + kBN > a.Nk) || (a.causal && key0 + kBN - 1 > a.q_start + q_row0 + t * kBM);
@@ -423,16 +506,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         alpha = ex2(m_run - m_use);  // 0 on the first tile
       }
       // Rescale this row of O when the reference max moved (not on the first
-      // tile: O is written, not accumulated, by the first PV).
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        for (int c = 0; c < D; c += 32) {
-          uint32_t u[32];
-          tmem_ld32(o_tm + c, u);
+      // tile: O is written, not accumulated, by the first PV).  With S prefetch
+      // this waits for the previous P V product (below, before P_t is written).
+      const auto rescale_o = [&]() {
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          for (int c = 0; c < D; c += 32) {
+            uint32_t u[32];
+            tmem_ld32(o_tm + c, u);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-          tmem_st32(o_tm + c, u);
+            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+            tmem_st32(o_tm + c, u);
+          }
         }
-      }
+      };
+      if constexpr (!kSPrefetch) rescale_o();
       const float neg_m = (m_use == -INFINITY) ? 0.f : -m_use;
       const float2 sl2x2 = make_float2(sl2, sl2), negm2 = make_float2(neg_m, neg_m);
       float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -453,12 +540,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             x[k0 + 1] = p1 - __uint_as_float(u[i] & 0xFFFF0000u);
           }
         }
-        tmem_st32(s_tm + half * 32, u);
+        if constexpr (kSPrefetch) {
+          if (half == 0) {
+            // P_t(j - 1) V(j - 1) must have read P_t (and finished adding into O_t)
+            // before P_t is overwritten or O_t rescaled; the first half's
+            // exponentials above overlap that product.
+            if (step > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars.pv_done[t], (step - 1) & 1, &bars.abort,
+                                                              &g_fwd_status))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            rescale_o();
+          }
+        }
+        tmem_st32(p_tm + half * 32, u);
         if (!kPrecise && half == 0) {  // keys 0..63 are ready for the PV product
           tc_fence_before();
           mbar_arrive_warp(&bars.p_half[t]);
         }
       }
+      if (!ok) break;
       if (kPrecise) {  // residuals over columns 64..127 (the S values there are consumed)
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -494,7 +596,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     // ------------------------------------------------------------ epilogue
     // The whole O row leaves tensor memory first; o_empty then lets the next item's
     // first P V product overwrite it while this row is normalised and stored.
-    if (!ok || !__all_sync(0xffffffffu, mbar_wait(&bars.o_full[t], it & 1, &bars.abort, &g_fwd_status, a.wait_ns))) {
+    if (!ok || !__all_sync(0xffffffffu, mbar_wait(&bars.o_full[t], it & 1, &bars.abort, &g_fwd_status))) {
       ok = false;
       break;
     }

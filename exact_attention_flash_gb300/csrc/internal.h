@@ -10,10 +10,6 @@
 
 namespace fa {
 
-// Wall-clock limit of a kernel's wait on its own pipeline (one second: every such
-// wait is on work the same CTA issued microseconds earlier).  fa_debug_next_wait_limit
-// replaces it for one call.
-constexpr unsigned long long kDefaultWaitNs = 1000000000ull;
 
 struct ForwardArgs {
   CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps over [B*H, Nq or Nk, d] bf16, box {64, 128, 1}, 128B swizzle
@@ -29,7 +25,7 @@ struct ForwardArgs {
                                  // on the stream before the launch
   int head_group;                // heads interleaved in the work order (set by the API, see head_group_for)
   unsigned long long* stats;     // optional counters [tiles, skipped, rescales, dq adds]; null: none
-  unsigned long long wait_ns;    // limit of each pipeline wait (kDefaultWaitNs unless a test shortens it)
+  int debug_abort;               // failure-path test: the kernel aborts as after a timed-out wait
 };
 
 struct BackwardArgs {
@@ -56,7 +52,7 @@ struct BackwardArgs {
   int o_f32;
   int head_group;                       // heads interleaved in the grid order (set by the API, see head_group_for)
   unsigned long long* stats;            // optional counters [tiles, skipped, rescales, dq adds]; null: none
-  unsigned long long wait_ns;           // limit of each pipeline wait (kDefaultWaitNs unless a test shortens it)
+  int debug_abort;                      // failure-path test: the kernel aborts as after a timed-out wait
 };
 
 // Heads whose blocks are interleaved in the work order.  Under causality a block's

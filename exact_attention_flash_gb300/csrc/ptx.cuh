@@ -112,25 +112,30 @@ __device__ __forceinline__ void mbar_arrive_warp(uint64_t* bar) {
 }
 
 // Wait until the barrier's phase with the given parity has completed.
-// Returns false (and raises *abort, sets kDevTimeout in *status) once `limit_ns`
-// has passed since the wait began, or false at once if another role of the CTA
-// has already raised *abort.  The deadline is tested before each sleeping try, so
-// a limit of 0 gives up as soon as the phase is found incomplete (the failure-path
-// tests use that to make a real kernel abort deterministically).
+// Returns false (and raises *abort, sets kDevTimeout in *status) on timeout,
+// or false at once if another role of the CTA has already raised *abort.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           unsigned* status,
                                           unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   while (true) {
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if (*abort) return false;
-    if (global_timer_ns() - t0 >= limit_ns) {
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort = 1;
       atomicOr(status, kDevTimeout);
       return false;
     }
-    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
   }
+}
+
+// What a timed-out wait does, done on purpose (the failure-path test hook): raise the
+// CTA's abort flag and record the timeout bit.  The other roles then leave their loops
+// through their own waits, as after a real timeout.
+__device__ __forceinline__ void raise_abort(volatile int* abort, unsigned* status) {
+  *abort = 1;
+  atomicOr(status, kDevTimeout);
 }
 
 // Wait without raising the abort flag: used while draining after an abort.
@@ -275,9 +280,8 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar, uint32_t leader) {
 }
 
 // Warp-uniform bounded wait: every lane waits, and all lanes agree on the outcome.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* status,
-                                          unsigned long long limit_ns = kWaitLimitNs) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, status, limit_ns));
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* status) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, status));
 }
 
 // Load 32 consecutive 32-bit columns of this thread's TMEM lane (warp-wide),

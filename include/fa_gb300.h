@@ -329,20 +329,17 @@ fa_status fa_set_stats(unsigned long long* counters);
 fa_status fa_debug_wait_timeout(unsigned long long limit_ns, void* stream);
 
 /*
- * fa_debug_next_wait_limit — test hook for the failure path of the real kernels:
+ * fa_debug_abort_next_call — test hook for the failure path of the real kernels:
  * the next fa_forward, fa_forward_qk, fa_backward or fa_backward_qk call made
- * from the calling host thread bounds each of its kernels' waits on their own
- * pipeline by `limit_ns` nanoseconds instead of one second (the deadline is
- * tested before each sleep, so 0 gives up the first time a wait finds its
- * barrier phase incomplete).  When a wait gives up, the kernel raises its abort
- * flag, every role leaves its loop, the copies and products already issued are
- * waited for (with the normal one-second limit), tensor memory is freed and the
- * kernel returns; that call's outputs are undefined and the next
- * fa_get_device_status() reports FA_ERR_TIMEOUT.  The limit is taken by that one
- * call; a second call of this function before it replaces the pending limit.
- * More than 5 s is FA_ERR_INVALID_ARG.
+ * from the calling host thread runs its kernel as if a wait on its own pipeline
+ * had timed out at the start (the MMA-issuing role raises the CTA's abort flag and
+ * records the timeout).  Every other role then leaves its loop through its own
+ * bounded wait, the copies and products already issued are waited for, tensor
+ * memory is freed and the kernel returns; that call's outputs are undefined and
+ * the next fa_get_device_status() reports FA_ERR_TIMEOUT.  The flag is taken by
+ * that one call.  Returns FA_OK.
  */
-fa_status fa_debug_next_wait_limit(unsigned long long limit_ns);
+fa_status fa_debug_abort_next_call(void);
 
 #ifdef __cplusplus
 }

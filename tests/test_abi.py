@@ -95,14 +95,6 @@ def test_forward_rejects_bad_arguments(lib):
     assert lib.fa_forward(FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 1, 8, 64, 0.0, 0, 0, FAKE + 4, 256, None) == 5
 
 
-def test_wait_limit_hook_arguments(lib):
-    # more than 5 s is refused; nothing is launched by these calls.  The last call
-    # sets the normal one-second limit, so no later test inherits a short one.
-    assert lib.fa_debug_next_wait_limit(5_000_000_001) == 1
-    assert lib.fa_debug_next_wait_limit(0) == 0
-    assert lib.fa_debug_next_wait_limit(1_000_000_000) == 0
-
-
 def test_backward_rejects_bad_arguments(lib):
     # fa_backward(q, k, v, o, o_dtype, lse, dout, dq, dk, dv, grad_dtype, B, H, N, d, scale, causal, ws, bytes, stream)
     args = [FAKE] * 4 + [0, FAKE, FAKE, FAKE, FAKE, FAKE]

@@ -110,6 +110,8 @@ def test_oracle_parity_leg_reports_errors_against_the_bars():
                     "inputs": {"q": qd, "k": kd, "v": vd}, "gpu": {"o": od, "lse": ld[..., 0]}},
         }
 
+    # shapes as the bench keeps them: decode O [heads, 1, d], LSE [heads]
+    assert od.shape == (3, 1, 64) and ld[..., 0].shape == (3,)
     ok = bench.oracle_parity(samples())
     assert ok["fb"]["within_bars"] and ok["dec"]["within_bars"]
     assert ok["fb"]["o_max_abs"] < 1e-12 and ok["fb"]["dk_rel_fro"] < 1e-12

@@ -3,11 +3,11 @@
 A kernel whose wait runs out returns on its own, the host reads FA_ERR_TIMEOUT,
 and the context stays usable.  Two forms:
 - a probe kernel that waits on a barrier nothing completes;
-- the real forward and backward kernels, made to give up through
-  fa_debug_next_wait_limit(0): the first wait that finds its barrier phase
-  incomplete raises the abort flag, every role leaves its loop, drains the copies
-  and products it issued, frees tensor memory and returns.  A normal call after it
-  must still match the oracle.
+- the real forward and backward kernels, made to abort through
+  fa_debug_abort_next_call(): the MMA-issuing role acts as if its first wait had
+  timed out and raises the abort flag; every other role leaves its loop through its
+  own bounded wait, drains the copies and products it issued, frees tensor memory
+  and returns.  A normal call after it must still match the oracle.
 """
 import numpy as np
 import pytest
@@ -45,8 +45,8 @@ def test_wait_timeout_is_reported_and_context_survives():
 
 @pytest.mark.parametrize("d", [64, 128])
 def test_forward_abort_path_then_normal_call(d):
-    """The persistent forward (B = H = 1, N = 256) with a zero wait limit comes back
-    with FA_ERR_TIMEOUT; the next call on the same buffers and workspace is exact."""
+    """The persistent forward (B = H = 1, N = 256), made to abort, comes back with
+    FA_ERR_TIMEOUT; the next call on the same buffers and workspace is exact."""
     from exact_attention_flash_gb300 import _lib, fa_forward, fa_get_device_status, forward_workspace_bytes
     from exact_attention_flash_gb300.workloads import make_attention_inputs
 
@@ -56,7 +56,7 @@ def test_forward_abort_path_then_normal_call(d):
     ws = torch.empty(forward_workspace_bytes(1, 1, 256, d, True), device="cuda", dtype=torch.uint8)
     o = torch.empty((1, 1, 256, d), device="cuda", dtype=torch.float32)
     lse = torch.empty((1, 1, 256), device="cuda")
-    assert lib.fa_debug_next_wait_limit(0) == 0
+    assert lib.fa_debug_abort_next_call() == 0
     fa_forward(q, k, v, causal=True, out=o, lse=lse, workspace=ws)
     torch.cuda.synchronize()
     assert fa_get_device_status() == FA_ERR_TIMEOUT
@@ -71,8 +71,8 @@ def test_forward_abort_path_then_normal_call(d):
 
 @pytest.mark.parametrize("d", [64, 128])
 def test_backward_abort_path_then_normal_call(d):
-    """The backward (preprocess + main kernel, B = H = 1, N = 256) with a zero wait
-    limit comes back with FA_ERR_TIMEOUT; the next call is exact."""
+    """The backward (preprocess + main kernel, B = H = 1, N = 256), made to abort,
+    comes back with FA_ERR_TIMEOUT; the next call is exact."""
     from exact_attention_flash_gb300 import _lib, fa_backward, fa_forward, fa_get_device_status
     from exact_attention_flash_gb300.workloads import make_attention_inputs
 
@@ -81,7 +81,7 @@ def test_backward_abort_path_then_normal_call(d):
     o, lse = fa_forward(q, k, v, causal=True)
     torch.cuda.synchronize()
     assert fa_get_device_status() == 0
-    assert lib.fa_debug_next_wait_limit(0) == 0
+    assert lib.fa_debug_abort_next_call() == 0
     fa_backward(q, k, v, o, lse, do, causal=True)
     torch.cuda.synchronize()
     assert fa_get_device_status() == FA_ERR_TIMEOUT
@@ -96,14 +96,14 @@ def test_backward_abort_path_then_normal_call(d):
         assert rel_fro(g, r) <= GRAD_REL_FRO, name
 
 
-def test_wait_limit_applies_to_one_call_only():
-    """The limit is taken by the next call: the call after it runs normally."""
+def test_abort_flag_applies_to_one_call_only():
+    """The flag is taken by the next call: the calls after it run normally."""
     from exact_attention_flash_gb300 import _lib, fa_forward, fa_get_device_status
     from exact_attention_flash_gb300.workloads import make_attention_inputs
 
     lib = _lib.load()
     q, k, v, _ = make_attention_inputs(2, 2, 300, 128, 320, "cuda", with_do=False)
-    assert lib.fa_debug_next_wait_limit(0) == 0
+    assert lib.fa_debug_abort_next_call() == 0
     fa_forward(q, k, v)
     torch.cuda.synchronize()
     assert fa_get_device_status() == FA_ERR_TIMEOUT
