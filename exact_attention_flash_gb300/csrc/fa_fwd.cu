@@ -230,12 +230,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             }
             uint8_t* k_dst = sK + s * C::kTileBytes;
             uint8_t* v_dst = sV + s * C::kTileBytes;
-            mbar_arrive_expect_tx(&bars.k_full[s], C::kTileBytes);
+            // With S prefetch K and V of a key tile land on one barrier: the issuer then
+            // tests one barrier per step (each test of an mbarrier costs it a few
+            // hundred cycles while the tensor core streams operands from shared memory).
+            uint64_t* v_bar = kSPrefetch ? &bars.k_full[s] : &bars.v_full[s];
+            mbar_arrive_expect_tx(&bars.k_full[s], kSPrefetch ? 2 * C::kTileBytes : C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c)
               tma_load_3d(k_dst + c * (kBN * 128), &a.tm_k, &bars.k_full[s], c * 64, j * kBN, w.bh);
-            mbar_arrive_expect_tx(&bars.v_full[s], C::kTileBytes);
+            if (!kSPrefetch) mbar_arrive_expect_tx(v_bar, C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c)
-              tma_load_3d(v_dst + c * (kBN * 128), &a.tm_v, &bars.v_full[s], c * 64, j * kBN, w.bh);
+              tma_load_3d(v_dst + c * (kBN * 128), &a.tm_v, v_bar, c * 64, j * kBN, w.bh);
             ++g;
           }
         }
@@ -245,7 +249,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         for (int gg = max(0, g - C::kStages); gg < g; ++gg) {
           const int s = gg % C::kStages;
           mbar_wait_drain(&bars.k_full[s], (gg / C::kStages) & 1);
-          mbar_wait_drain(&bars.v_full[s], (gg / C::kStages) & 1);
+          if (!kSPrefetch) mbar_wait_drain(&bars.v_full[s], (gg / C::kStages) & 1);
         }
       }
       __syncwarp();
@@ -279,13 +283,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           const uint32_t o_tm = tmem + C::kOCol + t * D;
           const uint32_t p_tm = kSPrefetch ? tmem + C::kPCol + t * (kBN / 2) : tmem + t * kBN;
           const uint32_t acc0 = first ? 0u : 1u;
-          if (!warp_wait(&bars.p_half[t], step & 1, &bars.abort, &g_fwd_status)) return false;
-          tc_fence_after();
+          if (!kSPrefetch) {
+            if (!warp_wait(&bars.p_half[t], step & 1, &bars.abort, &g_fwd_status)) return false;
+            tc_fence_after();
+          } else {  // with S prefetch the next S_t does not wait for this product: one hand-off
+            if (!warp_wait(&bars.p_full[t], step & 1, &bars.abort, &g_fwd_status)) return false;
+            tc_fence_after();
+          }
   #pragma unroll
           for (int kk = 0; kk < kBN / 32; ++kk)
             umma_ts(o_tm, p_tm + kk * 8, desc_add(v_d, kk * 16 * 128), kIdO, kk > 0 ? 1u : acc0, leader);
-          if (!warp_wait(&bars.p_full[t], step & 1, &bars.abort, &g_fwd_status)) return false;
-          tc_fence_after();
+          if (!kSPrefetch) {
+            if (!warp_wait(&bars.p_full[t], step & 1, &bars.abort, &g_fwd_status)) return false;
+            tc_fence_after();
+          }
   #pragma unroll
           for (int kk = kBN / 32; kk < kBN / 16; ++kk)
             umma_ts(o_tm, p_tm + kk * 8, desc_add(v_d, kk * 16 * 128), kIdO, 1u, leader);
@@ -335,11 +346,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             for (int j = 0; ok && j < w.n_kv[kTiles - 1]; ++j, ++g) {
               const int s = g % C::kStages, sn = (g + 1) % C::kStages;
               const uint32_t phn = ((g + 1) / C::kStages) & 1;
-              // S_t(j + 1) once the softmax has loaded S_t(j) and K(j + 1) has landed.
+              // S_t(j + 1) once the softmax has loaded S_t(j) and K(j + 1) has landed (V(j)
+              // landed with K(j), which the previous step waited for).
+              if (j + 1 < w.n_kv[kTiles - 1] && !warp_wait(&bars.k_full[sn], phn, &bars.abort, &g_fwd_status)) {
+                ok = false;
+                break;
+              }
               for (int t = 0; t < kTiles; ++t) {
                 if (j + 1 >= w.n_kv[t]) continue;
-                if (!warp_wait(&bars.k_full[sn], phn, &bars.abort, &g_fwd_status) ||
-                    !warp_wait(&bars.s_free[t], (step[t] + j) & 1, &bars.abort, &g_fwd_status)) {
+                if (!warp_wait(&bars.s_free[t], (step[t] + j) & 1, &bars.abort, &g_fwd_status)) {
                   ok = false;
                   break;
                 }
@@ -347,11 +362,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
                 issue_s(t, sn);
                 if (j + 2 == w.n_kv[t]) umma_commit(&bars.q_empty[t], leader);  // the item's last S_t
               }
-              if (!ok ||
-                  !warp_wait(&bars.v_full[s], (g / C::kStages) & 1, &bars.abort, &g_fwd_status)) {
-                ok = false;
-                break;
-              }
+              if (!ok) break;
               // O_t += P_t(j) V(j) once the softmax has written P_t(j).
               for (int t = 0; t < kTiles; ++t) {
                 if (j >= w.n_kv[t]) continue;  // tile 0 may need one key tile fewer
@@ -466,13 +477,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       tc_fence_after();
       float x[kBN];
       {
-        uint32_t u[64];
-        tmem_ld64(s_tm, u);
+        uint32_t ua[64], ub[64];
+        tmem_ld64x2(s_tm, s_tm + 64, ua, ub);  // the whole row of S_t, one wait
 #pragma unroll
-        for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(u[i]);
-        tmem_ld64(s_tm + 64, u);
-#pragma unroll
-        for (int i = 0; i < 64; ++i) x[64 + i] = __uint_as_float(u[i]);
+        for (int i = 0; i < 64; ++i) {
+          x[i] = __uint_as_float(ua[i]);
+          x[64 + i] = __uint_as_float(ub[i]);
+        }
       }
       if constexpr (kSPrefetch) {  // S_t is in registers: the next S_t product may overwrite it
         tc_fence_before();
@@ -523,8 +534,39 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       const float neg_m = (m_use == -INFINITY) ? 0.f : -m_use;
       const float2 sl2x2 = make_float2(sl2, sl2), negm2 = make_float2(neg_m, neg_m);
       float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      // P as packed bf16 pairs over the first 64 columns of S (keys 2c, 2c+1 in
-      // column c); every S value is already in registers.
+      // P as packed bf16 pairs over the first 64 columns of S, or over P_t's own
+      // columns with S prefetch (keys 2c, 2c+1 in column c); every S value is already
+      // in registers.
+      if constexpr (kSPrefetch) {
+        const auto p_of_half = [&](int half, uint32_t (&u)[32]) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int k0 = half * 64 + 2 * i;
+            const float2 e = __ffma2_rn(make_float2(x[k0], x[k0 + 1]), sl2x2, negm2);
+            const float p0 = ex2(e.x), p1 = ex2(e.y);
+            u[i] = pack_bf16(p0, p1);
+            sum2[i & 3] = __fadd2_rn(sum2[i & 3], make_float2(p0, p1));
+          }
+        };
+        uint32_t u0[32], u1[32];
+        p_of_half(0, u0);
+        // P_t(j - 1) V(j - 1) must have read P_t (and finished adding into O_t) before
+        // P_t is overwritten or O_t rescaled; the first half's exponentials above
+        // overlap that product.
+        if (step > 0 &&
+            !__all_sync(0xffffffffu, mbar_wait(&bars.pv_done[t], (step - 1) & 1, &bars.abort, &g_fwd_status))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        rescale_o();
+        // The first half's store lands while the second half is computed; one wait
+        // covers both before P_t is handed to the tensor core.
+        tmem_st32_nowait(p_tm, u0);
+        p_of_half(1, u1);
+        tmem_st32_nowait(p_tm + 32, u1);
+        tmem_wait_st();
+      } else {
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t u[32];
@@ -540,27 +582,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             x[k0 + 1] = p1 - __uint_as_float(u[i] & 0xFFFF0000u);
           }
         }
-        if constexpr (kSPrefetch) {
-          if (half == 0) {
-            // P_t(j - 1) V(j - 1) must have read P_t (and finished adding into O_t)
-            // before P_t is overwritten or O_t rescaled; the first half's
-            // exponentials above overlap that product.
-            if (step > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars.pv_done[t], (step - 1) & 1, &bars.abort,
-                                                              &g_fwd_status))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            rescale_o();
-          }
-        }
         tmem_st32(p_tm + half * 32, u);
         if (!kPrecise && half == 0) {  // keys 0..63 are ready for the PV product
           tc_fence_before();
           mbar_arrive_warp(&bars.p_half[t]);
         }
       }
-      if (!ok) break;
+      }
       if (kPrecise) {  // residuals over columns 64..127 (the S values there are consumed)
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
