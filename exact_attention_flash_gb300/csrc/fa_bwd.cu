@@ -189,6 +189,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     mbar_init(&sh.dkdv_full, 1);
     mbar_init(&sh.drain, 1);
     fence_barrier_init();
+    // The key tile's K and V go out at once: their latency overlaps the rest of the
+    // set-up (tensor-memory allocation, the ones tile).
+    tma_prefetch_desc(&a.tm_k);
+    tma_prefetch_desc(&a.tm_v);
+    mbar_arrive_expect_tx(&sh.kv_full, 2 * C::kKVBytes);
+    for (int c = 0; c < D / 64; ++c) {
+      tma_load_3d(sK + c * (kBKV * 128), &a.tm_k, &sh.kv_full, c * 64, key0, bh);
+      tma_load_3d(sV + c * (kBKV * 128), &a.tm_v, &sh.kv_full, c * 64, key0, bh);
+    }
   }
   // The ones tile, in the no-swizzle K-major layout of 8-row x 16-byte core matrices:
   // even core matrices hold columns 0-7 (1, 1, 1, 0, ...), odd ones columns 8-15 (0).
@@ -208,15 +217,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       // ------------------------------------------------------------ TMA producer
       if (lane == 0) {
         tma_prefetch_desc(&a.tm_q);
-        tma_prefetch_desc(&a.tm_k);
-        tma_prefetch_desc(&a.tm_v);
         tma_prefetch_desc(&a.tm_do);
-        mbar_arrive_expect_tx(&sh.kv_full, 2 * C::kKVBytes);
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d(sK + c * (kBKV * 128), &a.tm_k, &sh.kv_full, c * 64, key0, bh);
-          tma_load_3d(sV + c * (kBKV * 128), &a.tm_v, &sh.kv_full, c * 64, key0, bh);
-        }
-        // The bias tiles come from the preprocess kernel, which may still be running.
+        // (K and V were issued during set-up.)  The bias tiles come from the preprocess kernel, which may still be running.
         griddep_wait();
         int issued = 0;
         for (int n = 0; n < n_steps; ++n) {
@@ -515,7 +517,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         tma_store_3d(&a.tm_dk, sQ + (n_boxes + i) * kBoxBytes, box_cols * i, key0, bh);
       }
       asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-      asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+      // The CTA may leave once the staged boxes have been read out of shared memory;
+      // the global writes complete on their own (the grid's completion orders them
+      // before any later work on the stream).
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
     }
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kWriterRegs));

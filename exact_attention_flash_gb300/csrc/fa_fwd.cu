@@ -397,6 +397,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
                 ok = false;
                 break;
               }
+              bool k_next = false;  // K(j + 1) tested once per step (for the first tile that needs it)
               for (int t = 0; t < kTiles; ++t) {
                 if (j >= w.n_kv[t]) continue;  // tile 0 may need one key tile fewer
                 // The item's first P V_t overwrites O_t: the previous item's epilogue must
@@ -411,10 +412,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
                 }
                 if (t == kTiles - 1) umma_commit(&bars.kv_empty[s], leader);
                 if (j + 1 < w.n_kv[t]) {
-                  if (!warp_wait(&bars.k_full[sn], phn, &bars.abort, &g_fwd_status)) {
+                  if (!k_next && !warp_wait(&bars.k_full[sn], phn, &bars.abort, &g_fwd_status)) {
                     ok = false;
                     break;
                   }
+                  k_next = true;
                   tc_fence_after();
                   issue_s(t, sn);
                 } else {
@@ -477,13 +479,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       tc_fence_after();
       float x[kBN];
       {
-        uint32_t ua[64], ub[64];
-        tmem_ld64x2(s_tm, s_tm + 64, ua, ub);  // the whole row of S_t, one wait
+        uint32_t u[64];
+        tmem_ld64(s_tm, u);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          x[i] = __uint_as_float(ua[i]);
-          x[64 + i] = __uint_as_float(ub[i]);
-        }
+        for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(u[i]);
+        tmem_ld64(s_tm + 64, u);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) x[64 + i] = __uint_as_float(u[i]);
       }
       if constexpr (kSPrefetch) {  // S_t is in registers: the next S_t product may overwrite it
         tc_fence_before();
