@@ -64,6 +64,10 @@ constexpr int kComputeRegs = 120;
 constexpr int kWriterRegs = 72;
 constexpr int kOtherRegs = 96;
 constexpr int kRegsNeeded = 256 * kComputeRegs + 256 * kWriterRegs + 128 * kOtherRegs;
+// dQ writer warps that read each step's dQ^T: all eight at d = 128; at d = 64 the four
+// whose lane quarters hold that step's features (see the dQ writers).
+template <int D>
+constexpr int kDqWarpsPerStep = D == 64 ? 4 : 8;
 
 template <int D>
 struct BwdCfg {
@@ -122,9 +126,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sK = smem;
-  uint8_t* sV = sK + C::kKVBytes;
-  uint8_t* sQ = sV + C::kKVBytes;                       // [kStages][kQBytes]
+  // K and V tiles.  At d = 64 V comes first: the A operand of dQ^T = K^T dS^T is K
+  // in MN-major form, M = 128 rows of which d = 64 are features; with K right after
+  // V, a descriptor that starts at V and puts its second 64-row chunk at K lands
+  // dQ^T in TMEM lanes 64..127 (see the dQ writers).
+  uint8_t* sV = smem + (D == 64 ? 0 : C::kKVBytes);
+  uint8_t* sK = smem + (D == 64 ? C::kKVBytes : 0);
+  uint8_t* sQ = smem + 2 * C::kKVBytes;                 // [kStages][kQBytes]
   uint8_t* sDO = sQ + C::kStages * C::kQBytes;          // [kStages][kQBytes]
   uint8_t* sDS = sDO + C::kStages * C::kQBytes;         // [2][kDSBytes]
   uint8_t* sBias = sDS + 2 * C::kDSBytes;               // [kStages][kBiasBytes]
@@ -183,7 +191,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       mbar_init(&sh.p_full[b], 8);   // one arrival per P/dS warp
       mbar_init(&sh.ds_full[b], 8);
       mbar_init(&sh.dq_full[b], 1);
-      mbar_init(&sh.dq_empty[b], 8); // one arrival per dQ writer warp
+      mbar_init(&sh.dq_empty[b], kDqWarpsPerStep<D>);  // one arrival per dQ writer warp of the step
       mbar_init(&sh.ds_empty[b], 1);
     }
     mbar_init(&sh.dkdv_full, 1);
@@ -256,6 +264,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         const uint64_t dK_k = sdesc_sw128(smem_u32(sK), 16, 1024);          // K, K-major (A of S^T)
         const uint64_t dV_k = sdesc_sw128(smem_u32(sV), 16, 1024);          // V, K-major (A of dP^T)
         const uint64_t dK_mn = sdesc_sw128(smem_u32(sK), kBKV * 128, 1024); // K as MN-major A of dQ^T
+        // d = 64, odd steps: rows 0..63 read V (unused), rows 64..127 are K^T dS^T.
+        const uint64_t dK_mn_hi = sdesc_sw128(smem_u32(sV), C::kKVBytes, 1024);
         const uint64_t dQ_k = sdesc_sw128(smem_u32(sQ), 16, 1024);          // Q stage 0, K-major (B of S^T)
         const uint64_t dDO_k = sdesc_sw128(smem_u32(sDO), 16, 1024);        // dO stage 0, K-major (B of dP^T)
         const uint64_t dQ_mn = sdesc_sw128(smem_u32(sQ), kBQ * 128, 1024);  // Q stage 0, MN-major (B of dK)
@@ -334,12 +344,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
             umma_ts(tmem + C::kDKCol, s_tm + 128 + pcol(kk), desc_add(q_d, kk * 16 * 128), kIdKV, kk > 0 ? 1u : acc0, leader);
           umma_commit(&sh.q_empty[s], leader);
           // dQ_i^T = K^T dS^T into the dP^T buffer (its dS^T was consumed by the dK MMA above).
-          // A = K as an MN-major [d x keys] operand; for d = 64 the upper 64 rows of the
-          // M = 128 product read the V tile and are ignored.
+          // A = K as an MN-major [d x keys] operand.  For d = 64 only 64 of the M = 128
+          // rows are features: even steps put them in lanes 0..63 (the other rows read
+          // whatever follows K), odd steps in lanes 64..127 (the other rows read V), so
+          // that the two halves of the dQ writers take alternate steps.
           const uint64_t ds_d = desc_add(dDS_mn, b * C::kDSBytes);
+          const uint64_t dq_a = (D == 64 && (n & 1)) ? dK_mn_hi : dK_mn;
   #pragma unroll
           for (int kk = 0; kk < kBKV / 16; ++kk)
-            umma_ss(s_tm + 128, desc_add(dK_mn, kk * 16 * 128), desc_add(ds_d, kk * 16 * 128), kIdQ, kk > 0, leader);
+            umma_ss(s_tm + 128, desc_add(dq_a, kk * 16 * 128), desc_add(ds_d, kk * 16 * 128), kIdQ, kk > 0, leader);
           umma_commit(&sh.dq_full[b], leader);
           umma_commit(&sh.ds_empty[b], leader);
         }
@@ -529,28 +542,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     // writer warpgroup takes 32 of the 64 query columns and adds them into dQ with
     // fp32 reductions in L2, straight from registers: for each query, a warp's 32
     // lanes cover 128 contiguous bytes of the dQ row.
+    // d = 64: dQ^T of even steps is in lanes 0..63, of odd steps in lanes 64..127, so
+    // the warps of lane quarters 0-1 reduce the even steps and those of quarters 2-3 the
+    // odd ones: all eight warps work, each on every other step.
     const int half = (warp - kWriterWarp0) >> 2;  // query columns [32*half, 32*half + 32)
-    const int lane_base = (warp & 3) * 32;
-    const bool has_rows = lane_base < D;          // for d = 64, lanes 64..127 hold no feature
+    const int lane_base = (warp & 3) * 32;        // this warp's TMEM lanes
+    const int parity = D == 64 ? (warp & 3) >> 1 : -1;  // d = 64: the steps this warp takes
+    const int feat0 = D == 64 ? lane_base & 32 : lane_base;  // feature of this warp's lane 0
     griddep_wait();  // dQ is zeroed by the preprocess kernel, which may still be running
     unsigned n_added = 0;  // dQ elements this thread added (fa_set_stats counters)
     for (int n = 0; n < n_steps; ++n) {
       const int b = n & 1;
+      if (parity >= 0 && b != parity) continue;
       const int q0 = (i_start + n) * kBQ + 32 * half;
       if (!__all_sync(0xffffffffu, mbar_wait(&sh.dq_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status))) break;
       uint32_t v[32];
       tc_fence_after();
-      if (has_rows) tmem_ld32(tmem_addr(tmem, lane_base, 128 + b * kBQ + 32 * half), v);
+      tmem_ld32(tmem_addr(tmem, lane_base, 128 + b * kBQ + 32 * half), v);
       tc_fence_before();
       mbar_arrive_warp(&sh.dq_empty[b]);
-      if (has_rows) {
+      {
         // 4 x 4 transposes within each group of four lanes (two shuffle rounds per
         // block of four queries): lane 4g + i ends up with features 4g .. 4g + 3 of
         // queries 4k + i, which leave as 16-byte vector reductions.  One warp
         // instruction then covers four whole 128-byte row segments, a quarter of the
         // instructions of one reduction per feature.
         const int i4 = lane & 3;
-        const long long dst_idx = (static_cast<long long>(bh) * a.Nq + q0 + i4) * D + lane_base + 4 * (lane >> 2);
+        const long long dst_idx = (static_cast<long long>(bh) * a.Nq + q0 + i4) * D + feat0 + 4 * (lane >> 2);
         float* dst = a.dq + dst_idx;
         const int rows = min(32, a.Nq - q0);
         const long long dq_elems = static_cast<long long>(a.B) * a.H * a.Nq * D;
