@@ -423,21 +423,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       // S^T - LSE/scale (the bias came with the product).
       uint32_t sv[32];
       tmem_ld32(s_tm, sv);
+      // The exponentials are issued back to back (all arguments first, then all 32
+      // ex2, then the packs), so that the special-function unit's latency overlaps
+      // across them instead of each result being waited for by its pack.
       float p[32];
       uint32_t pk[16];
       const float2 sl2x2 = make_float2(sl2, sl2);
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
         const float2 arg = __fmul2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2x2);
-        p[e] = ex2(arg.x);
-        p[e + 1] = ex2(arg.y);
-        if (need_mask) {
-          const int qe = q0 + 32 * h + e;
-          if (!key_valid || qe < first_visible_q) p[e] = 0.f;
-          if (!key_valid || qe + 1 < first_visible_q) p[e + 1] = 0.f;
-        }
-        pk[e / 2] = pack_bf16(p[e], p[e + 1]);
+        p[e] = arg.x;
+        p[e + 1] = arg.y;
       }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) p[e] = ex2(p[e]);
+      if (need_mask) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (!key_valid || q0 + 32 * h + e < first_visible_q) p[e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) pk[e / 2] = pack_bf16(p[e], p[e + 1]);
       // P^T packed (queries 2c, 2c+1 in column c) over the first 16 of this half's 32
       // columns, which this thread has already read.
       tmem_st16(s_tm, pk);

@@ -536,20 +536,36 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       const float neg_m = (m_use == -INFINITY) ? 0.f : -m_use;
       const float2 sl2x2 = make_float2(sl2, sl2), negm2 = make_float2(neg_m, neg_m);
       float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      // P of keys [64 half, 64 half + 64): the arguments, then all 64 exponentials back to
+      // back (so that the special-function unit's latency overlaps across them instead of
+      // each result being waited for by its pack), then the packs and sums.  x keeps p,
+      // or with precise its bf16 rounding residual for the second P V product.
+      const auto exp_half = [&](int half, uint32_t (&u)[32]) {
+        float* xh = x + half * 64;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float2 e = __ffma2_rn(make_float2(xh[2 * i], xh[2 * i + 1]), sl2x2, negm2);
+          xh[2 * i] = e.x;
+          xh[2 * i + 1] = e.y;
+        }
+#pragma unroll
+        for (int k = 0; k < 64; ++k) xh[k] = ex2(xh[k]);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = xh[2 * i], p1 = xh[2 * i + 1];
+          u[i] = pack_bf16(p0, p1);
+          sum2[i & 3] = __fadd2_rn(sum2[i & 3], make_float2(p0, p1));
+          if (kPrecise) {  // keep the rounding residual for the second PV product
+            xh[2 * i] = p0 - __uint_as_float(u[i] << 16);
+            xh[2 * i + 1] = p1 - __uint_as_float(u[i] & 0xFFFF0000u);
+          }
+        }
+      };
       // P as packed bf16 pairs over the first 64 columns of S, or over P_t's own
       // columns with S prefetch (keys 2c, 2c+1 in column c); every S value is already
       // in registers.
       if constexpr (kSPrefetch) {
-        const auto p_of_half = [&](int half, uint32_t (&u)[32]) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int k0 = half * 64 + 2 * i;
-            const float2 e = __ffma2_rn(make_float2(x[k0], x[k0 + 1]), sl2x2, negm2);
-            const float p0 = ex2(e.x), p1 = ex2(e.y);
-            u[i] = pack_bf16(p0, p1);
-            sum2[i & 3] = __fadd2_rn(sum2[i & 3], make_float2(p0, p1));
-          }
-        };
+        const auto p_of_half = [&](int half, uint32_t (&u)[32]) { exp_half(half, u); };
         uint32_t u0[32], u1[32];
         p_of_half(0, u0);
         // P_t(j - 1) V(j - 1) must have read P_t (and finished adding into O_t) before
@@ -572,18 +588,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t u[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int k0 = half * 64 + 2 * i;
-          const float2 e = __ffma2_rn(make_float2(x[k0], x[k0 + 1]), sl2x2, negm2);
-          const float p0 = ex2(e.x), p1 = ex2(e.y);
-          u[i] = pack_bf16(p0, p1);
-          sum2[i & 3] = __fadd2_rn(sum2[i & 3], make_float2(p0, p1));
-          if (kPrecise) {  // keep the rounding residual for the second PV product
-            x[k0] = p0 - __uint_as_float(u[i] << 16);
-            x[k0 + 1] = p1 - __uint_as_float(u[i] & 0xFFFF0000u);
-          }
-        }
+        exp_half(half, u);
         tmem_st32(p_tm + half * 32, u);
         if (!kPrecise && half == 0) {  // keys 0..63 are ready for the PV product
           tc_fence_before();
