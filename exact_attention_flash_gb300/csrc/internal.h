@@ -58,13 +58,17 @@ struct BackwardArgs {
 // Heads whose blocks are interleaved in the work order.  Under causality a block's
 // work grows with its position, and interleaving heads lets the longest blocks of
 // several heads start first, which shortens the tail; the interleaved heads' K and V
-// (forward) or Q, dO and dQ (backward) must then share L2, so a group holds as many
-// heads as fit a 64 MB budget, at most 8, and the heads are split into groups of
-// equal size (a small last group would start its longest blocks late).  Without
-// causality every block has the same work and one head at a time keeps the most in L2.
+// (forward) or Q, dO and dQ (backward) must then share L2.  When every head's data
+// fits a 64 MB budget together, all heads form one group: the whole grid then runs
+// longest blocks first.  Otherwise a group holds as many heads as fit the budget, at
+// most 8, and the heads are split into groups of equal size (a small last group
+// would start its longest blocks late).  Without causality every block has the same
+// work and one head at a time keeps the most in L2.
 inline int head_group_for(int causal, long long bytes_per_head, int n_bh) {
   if (!causal || n_bh < 1) return 1;
-  long long fit = (64ll << 20) / (bytes_per_head > 0 ? bytes_per_head : 1);
+  constexpr long long kBudget = 64ll << 20;
+  if (bytes_per_head > 0 && static_cast<long long>(n_bh) <= kBudget / bytes_per_head) return n_bh;
+  long long fit = kBudget / (bytes_per_head > 0 ? bytes_per_head : 1);
   fit = fit < 1 ? 1 : (fit > 8 ? 8 : fit);
   const long long groups = (n_bh + fit - 1) / fit;
   return static_cast<int>((n_bh + groups - 1) / groups);
