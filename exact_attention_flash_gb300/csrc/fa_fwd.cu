@@ -78,12 +78,20 @@ struct FwdCfg {
   static constexpr int kSmemBytes = kTiles * kTileBytes + kStages * 2 * kTileBytes + 1024;
 };
 
+// One work item: kTiles * kBM query rows of one (batch, head), and the number of
+// key tiles each of its query tiles visits.
+struct FwdItem {
+  int bh, q_row0;
+  int n_kv[kTiles];
+};
+
 constexpr int kItemRing = 2;
 constexpr int kItemReaders = 1 + 2 * kBM / 32;  // arrivals per warp: the MMA warp and the softmax warps
 
 struct FwdBarriers {
   uint64_t item_full[kItemRing], item_empty[kItemRing];
   int item[kItemRing];
+  FwdItem work[kItemRing];  // the item's fields, computed once by the producer
   uint64_t q_full[kTiles], q_empty[kTiles];
   uint64_t k_full[4], v_full[4], kv_empty[4];
   uint64_t s_full[kTiles], p_half[kTiles], p_full[kTiles], o_full[kTiles], o_empty[kTiles];
@@ -91,13 +99,6 @@ struct FwdBarriers {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-};
-
-// One work item: kTiles * kBM query rows of one (batch, head), and the number of
-// key tiles each of its query tiles visits.
-struct FwdItem {
-  int bh, q_row0;
-  int n_kv[kTiles];
 };
 
 // Work items in dispatch order: heads in groups of a.head_group; within a group, the
@@ -206,10 +207,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             break;
           const unsigned claimed = atomicAdd(a.sched, 1u);
           const int item = claimed < static_cast<unsigned>(n_items) ? static_cast<int>(claimed) : n_items;
+          const FwdItem w = item < n_items ? fwd_item(a, item) : FwdItem{0, 0, {0, 0}};
+          // The readers take the item's fields from the ring rather than computing them:
+          // integer division by the run's sizes in an MMA issuer's code was measured to
+          // slow every step of its issue loop.
           bars.item[r] = item;
+          bars.work[r] = w;
           mbar_arrive(&bars.item_full[r]);
           if (item >= n_items) break;
-          const FwdItem w = fwd_item(a, item);
           // Q tile t is reloaded once the previous item's last S_t product has read it.
           for (int t = 0; ok && t < kTiles; ++t) {
             if (it > 0 && !mbar_wait(&bars.q_empty[t], (it - 1) & 1, &bars.abort, &g_fwd_status)) {
@@ -318,9 +323,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           const int r = it % kItemRing;
           if (!warp_wait(&bars.item_full[r], (it / kItemRing) & 1, &bars.abort, &g_fwd_status)) break;
           const int item = bars.item[r];
+          // (At d = 64 the issuer computes the item itself: taking it from the ring was
+          // 4 % slower there for long rows, 2 % faster at d = 128.)
+          const FwdItem w = kSPrefetch ? fwd_item(a, min(item, n_items - 1)) : bars.work[r];
           mbar_arrive_warp(&bars.item_empty[r]);
           if (item >= n_items) break;
-          const FwdItem w = fwd_item(a, item);
 #pragma unroll
           for (int t = 0; t < kTiles; ++t)
             if (w.q_row0 + t * kBM < a.Nq) {
@@ -461,9 +468,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     if (!__all_sync(0xffffffffu, mbar_wait(&bars.item_full[ring], (it / kItemRing) & 1, &bars.abort, &g_fwd_status)))
       break;
     const int item = bars.item[ring];
+    const FwdItem w = bars.work[ring];
     mbar_arrive_warp(&bars.item_empty[ring]);
     if (item >= n_items) break;
-    const FwdItem w = fwd_item(a, item);
     const int q_row0 = w.q_row0, bh = w.bh;
     const int row = q_row0 + t * kBM + r;
     float mx_seen = -INFINITY;  // true running max of the raw scores (counters only)
