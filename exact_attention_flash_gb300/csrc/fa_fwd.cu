@@ -198,6 +198,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         tma_prefetch_desc(&a.tm_v);
         int g = 0;                     // K/V tiles issued (the ring position)
         int q_issued[kTiles] = {0, 0};  // Q tiles issued per tile slot
+        // fa_set_stats counters: S products of query tiles that start before N, and
+        // the key tiles causality skipped for them (counted here, off the MMA issuer).
+        unsigned n_tiles = 0, n_skipped = 0;
+        const int n_kv_total = (a.Nk + kBN - 1) / kBN;
         bool ok = true;
         for (int it = 0; ok; ++it) {
           // Claim the next item and publish it (n_items once none is left).
@@ -215,6 +219,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           bars.work[r] = w;
           mbar_arrive(&bars.item_full[r]);
           if (item >= n_items) break;
+#pragma unroll
+          for (int t = 0; t < kTiles; ++t)
+            if (w.q_row0 + t * kBM < a.Nq) {
+              n_tiles += w.n_kv[t];
+              n_skipped += n_kv_total - w.n_kv[t];
+            }
           // Q tile t is reloaded once the previous item's last S_t product has read it.
           for (int t = 0; ok && t < kTiles; ++t) {
             if (it > 0 && !mbar_wait(&bars.q_empty[t], (it - 1) & 1, &bars.abort, &g_fwd_status)) {
@@ -255,6 +265,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           const int s = gg % C::kStages;
           mbar_wait_drain(&bars.k_full[s], (gg / C::kStages) & 1);
           if (!kSPrefetch) mbar_wait_drain(&bars.v_full[s], (gg / C::kStages) & 1);
+        }
+        if (a.stats != nullptr) {
+          if (n_tiles != 0u) atomicAdd(a.stats + 0, static_cast<unsigned long long>(n_tiles));
+          if (n_skipped != 0u) atomicAdd(a.stats + 1, static_cast<unsigned long long>(n_skipped));
         }
       }
       __syncwarp();
@@ -314,10 +328,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         };
         int g = 0;                  // K/V tiles consumed (the ring position)
         int step[kTiles] = {0, 0};  // per-tile steps before the current item
-        // fa_set_stats counters: S products of query tiles that start before N, and
-        // the key tiles causality skipped for them.
-        unsigned n_tiles = 0, n_skipped = 0;
-        const int n_kv_total = (a.Nk + kBN - 1) / kBN;
         bool ok = true;
         for (int it = 0; ok; ++it) {
           const int r = it % kItemRing;
@@ -328,12 +338,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           const FwdItem w = kSPrefetch ? fwd_item(a, min(item, n_items - 1)) : bars.work[r];
           mbar_arrive_warp(&bars.item_empty[r]);
           if (item >= n_items) break;
-#pragma unroll
-          for (int t = 0; t < kTiles; ++t)
-            if (w.q_row0 + t * kBM < a.Nq) {
-              n_tiles += w.n_kv[t];
-              n_skipped += n_kv_total - w.n_kv[t];
-            }
           const int s0 = g % C::kStages;
           ok = warp_wait(&bars.k_full[s0], (g / C::kStages) & 1, &bars.abort, &g_fwd_status);
           if constexpr (kSPrefetch) {
@@ -438,10 +442,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         // Drain: all MMAs complete before tensor memory is released.
         umma_commit(&bars.drain, leader);
         mbar_wait_drain(&bars.drain, 0);
-        if (a.stats != nullptr && lane == 0) {
-          if (n_tiles != 0u) atomicAdd(a.stats + 0, static_cast<unsigned long long>(n_tiles));
-          if (n_skipped != 0u) atomicAdd(a.stats + 1, static_cast<unsigned long long>(n_skipped));
-        }
       }
       __syncwarp();
     }
