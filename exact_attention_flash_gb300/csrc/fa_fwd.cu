@@ -333,9 +333,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           const int r = it % kItemRing;
           if (!warp_wait(&bars.item_full[r], (it / kItemRing) & 1, &bars.abort, &g_fwd_status)) break;
           const int item = bars.item[r];
-          // (At d = 64 the issuer computes the item itself: taking it from the ring was
-          // 4 % slower there for long rows, 2 % faster at d = 128.)
-          const FwdItem w = kSPrefetch ? fwd_item(a, min(item, n_items - 1)) : bars.work[r];
+          const FwdItem w = bars.work[r];
           mbar_arrive_warp(&bars.item_empty[r]);
           if (item >= n_items) break;
           const int s0 = g % C::kStages;
