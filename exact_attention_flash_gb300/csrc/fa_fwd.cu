@@ -93,7 +93,7 @@ struct FwdBarriers {
   int item[kItemRing];
   FwdItem work[kItemRing];  // the item's fields, computed once by the producer
   uint64_t q_full[kTiles], q_empty[kTiles];
-  uint64_t k_full[4], v_full[4], kv_empty[4];
+  uint64_t k_full[4], v_full[4], kv_empty[4], k_empty[4];  // k_empty: d = 128 (K released before V)
   uint64_t s_full[kTiles], p_half[kTiles], p_full[kTiles], o_full[kTiles], o_empty[kTiles];
   uint64_t s_free[kTiles], pv_done[kTiles];  // S-prefetch schedule only (d = 64)
   uint64_t drain;
@@ -168,6 +168,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       mbar_init(&bars.k_full[s], 1);
       mbar_init(&bars.v_full[s], 1);
       mbar_init(&bars.kv_empty[s], 1);
+      mbar_init(&bars.k_empty[s], 1);
     }
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(&bars.s_full[t], 1);
@@ -239,7 +240,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           }
           for (int j = 0; ok && j < w.n_kv[kTiles - 1]; ++j) {
             const int s = g % C::kStages;
-            if (g >= C::kStages && !mbar_wait(&bars.kv_empty[s], ((g / C::kStages) - 1) & 1, &bars.abort, &g_fwd_status)) {
+            // d = 128: K of a stage is released once both tiles' S products have read it,
+            // V once both P V products have; K then loads about a step before V, so the
+            // next S product does not wait for its K.
+            if (g >= C::kStages &&
+                !mbar_wait(kSPrefetch ? &bars.kv_empty[s] : &bars.k_empty[s], ((g / C::kStages) - 1) & 1, &bars.abort,
+                           &g_fwd_status)) {
               ok = false;
               break;
             }
@@ -252,7 +258,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             mbar_arrive_expect_tx(&bars.k_full[s], kSPrefetch ? 2 * C::kTileBytes : C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c)
               tma_load_3d(k_dst + c * (kBN * 128), &a.tm_k, &bars.k_full[s], c * 64, j * kBN, w.bh);
-            if (!kSPrefetch) mbar_arrive_expect_tx(v_bar, C::kTileBytes);
+            if (!kSPrefetch) {
+              if (g >= C::kStages &&
+                  !mbar_wait(&bars.kv_empty[s], ((g / C::kStages) - 1) & 1, &bars.abort, &g_fwd_status)) {
+                mbar_wait_drain(&bars.k_full[s], (g / C::kStages) & 1);  // the K copy just issued lands first
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(v_bar, C::kTileBytes);
+            }
             for (int c = 0; c < C::kChunks; ++c)
               tma_load_3d(v_dst + c * (kBN * 128), &a.tm_v, v_bar, c * 64, j * kBN, w.bh);
             ++g;
@@ -398,6 +412,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
               }
               tc_fence_after();
               issue_s(t, s0);
+              if (t == kTiles - 1) umma_commit(&bars.k_empty[s0], leader);  // both S products have read K
             }
             for (int j = 0; ok && j < w.n_kv[kTiles - 1]; ++j, ++g) {
               const int s = g % C::kStages, sn = (g + 1) % C::kStages;
@@ -428,6 +443,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
                   k_next = true;
                   tc_fence_after();
                   issue_s(t, sn);
+                  if (t == kTiles - 1) umma_commit(&bars.k_empty[sn], leader);  // both S products have read K
                 } else {
                   umma_commit(&bars.o_full[t], leader);   // O_t of this item is complete
                   umma_commit(&bars.q_empty[t], leader);  // its last S_t product has read Q_t
@@ -514,8 +530,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         mx8[c] = fmaxf(v, x[16 * c + 15]);
       }
       const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-      n_rescales += (row < a.Nq && mx > mx_seen && mx_seen != -INFINITY) ? 1u : 0u;
-      mx_seen = fmaxf(mx_seen, mx);
+      if (a.stats != nullptr) {  // counters only (a uniform branch on a kernel argument)
+        n_rescales += (row < a.Nq && mx > mx_seen && mx_seen != -INFINITY) ? 1u : 0u;
+        mx_seen = fmaxf(mx_seen, mx);
+      }
       const float m_tile = mx * sl2;
       float m_use = m_run;
       float alpha = 1.f;
