@@ -16,7 +16,8 @@
 //   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into TMEM (SS MMA),
 //               O_t += P_t V_j with P read from TMEM (TS MMA), interleaving the
 //               two tiles so the tensor core works on one tile while the other
-//               tile's softmax runs.
+//               tile's softmax runs.  With d = 64 it issues the S products only,
+//               and warps 10 and 11 issue tile 0's and tile 1's P V products.
 //   warps 0-3   softmax for tile 0, warps 4-7 for tile 1: thread r owns query
 //               row r (TMEM lane r), loads its row of S, takes the row max in
 //               registers, writes P as bf16 over the S columns, and rescales its
@@ -47,7 +48,7 @@ constexpr int kBN = 128;             // keys per KV tile
 constexpr int kTiles = 2;            // query tiles per CTA
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kFwdThreads = 384;  // warps 10-11 only lend their registers to the softmax warps
+constexpr int kFwdThreads = 384;  // warps 10-11: the P V issuers at d = 64; otherwise they only lend registers
 // Register split (setmaxnreg): softmax warpgroups 0-1 raise their budget, warpgroup 2
 // (producer, MMA issuer, two idle warps) lowers it.  The sum must stay within what
 // the CTA was launched with; the launcher checks this against the compiled kernel.
@@ -80,6 +81,7 @@ struct FwdCfg {
 
 // One work item: kTiles * kBM query rows of one (batch, head), and the number of
 // key tiles each of its query tiles visits.
+constexpr int kPvWarp0 = 10;  // with S prefetch, warps 10 and 11 issue tile 0's and tile 1's P V products
 struct FwdItem {
   int bh, q_row0;
   int n_kv[kTiles];
@@ -96,7 +98,7 @@ struct FwdBarriers {
   uint64_t k_full[4], v_full[4], kv_empty[4], k_empty[4];  // k_empty: d = 128 (K released before V)
   uint64_t s_full[kTiles], p_half[kTiles], p_full[kTiles], o_full[kTiles], o_empty[kTiles];
   uint64_t s_free[kTiles], pv_done[kTiles];  // S-prefetch schedule only (d = 64)
-  uint64_t drain;
+  uint64_t drain, drain_pv[kTiles];
   uint32_t tmem_base;
   int abort;
 };
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     bars.abort = 0;
     for (int r = 0; r < kItemRing; ++r) {
       mbar_init(&bars.item_full[r], 1);
-      mbar_init(&bars.item_empty[r], kItemReaders);
+      mbar_init(&bars.item_empty[r], kItemReaders + (kSPrefetch ? kTiles : 0));
     }
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(&bars.q_full[t], 1);
@@ -167,7 +169,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars.k_full[s], 1);
       mbar_init(&bars.v_full[s], 1);
-      mbar_init(&bars.kv_empty[s], 1);
+      // With S prefetch a stage is released by the issuer's S products and by each
+      // tile's P V product (issued by that tile's softmax warps).
+      mbar_init(&bars.kv_empty[s], kSPrefetch ? 1 + kTiles : 1);
       mbar_init(&bars.k_empty[s], 1);
     }
     for (int t = 0; t < kTiles; ++t) {
@@ -178,6 +182,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       mbar_init(&bars.s_free[t], kBM / 32);
       mbar_init(&bars.pv_done[t], 1);
     }
+    for (int t = 0; t < kTiles; ++t) mbar_init(&bars.drain_pv[t], 1);
     mbar_init(&bars.drain, 1);
     fence_barrier_init();
   }
@@ -353,6 +358,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           const int s0 = g % C::kStages;
           ok = warp_wait(&bars.k_full[s0], (g / C::kStages) & 1, &bars.abort, &g_fwd_status);
           if constexpr (kSPrefetch) {
+            // S products only: each tile's softmax warps issue their own P V products.
+            // Stage s of the K/V ring is released once the S products that read K and
+            // both tiles' P V products that read V have completed; this thread arrives
+            // once for its S products and once more for each tile that has no P V with
+            // that key tile (tile 0 may need one key tile fewer).
+            const auto release_kv = [&](int jj, int stage) {
+              umma_commit(&bars.kv_empty[stage], leader);
+              for (int t = 0; t < kTiles; ++t)
+                if (jj >= w.n_kv[t]) umma_commit(&bars.kv_empty[stage], leader);
+            };
             // The item's first S_t: Q_t reloaded, and S_t of the previous item's last
             // step loaded by the softmax.
             for (int t = 0; ok && t < kTiles; ++t) {
@@ -366,12 +381,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
               issue_s(t, s0);
               if (w.n_kv[t] == 1) umma_commit(&bars.q_empty[t], leader);  // its only S_t has read Q_t
             }
-            for (int j = 0; ok && j < w.n_kv[kTiles - 1]; ++j, ++g) {
-              const int s = g % C::kStages, sn = (g + 1) % C::kStages;
+            if (ok) release_kv(0, s0);
+            for (int j = 0; ok && j + 1 < w.n_kv[kTiles - 1]; ++j, ++g) {
+              const int sn = (g + 1) % C::kStages;
               const uint32_t phn = ((g + 1) / C::kStages) & 1;
-              // S_t(j + 1) once the softmax has loaded S_t(j) and K(j + 1) has landed (V(j)
-              // landed with K(j), which the previous step waited for).
-              if (j + 1 < w.n_kv[kTiles - 1] && !warp_wait(&bars.k_full[sn], phn, &bars.abort, &g_fwd_status)) {
+              // S_t(j + 1) once the softmax has loaded S_t(j) and K(j + 1) has landed.
+              if (!warp_wait(&bars.k_full[sn], phn, &bars.abort, &g_fwd_status)) {
                 ok = false;
                 break;
               }
@@ -385,25 +400,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
                 issue_s(t, sn);
                 if (j + 2 == w.n_kv[t]) umma_commit(&bars.q_empty[t], leader);  // the item's last S_t
               }
-              if (!ok) break;
-              // O_t += P_t(j) V(j) once the softmax has written P_t(j).
-              for (int t = 0; t < kTiles; ++t) {
-                if (j >= w.n_kv[t]) continue;  // tile 0 may need one key tile fewer
-                if (j == 0 && it > 0 &&
-                    !warp_wait(&bars.o_empty[t], (it - 1) & 1, &bars.abort, &g_fwd_status)) {
-                  ok = false;
-                  break;
-                }
-                if (!issue_pv(t, s, step[t] + j, j == 0)) {
-                  ok = false;
-                  break;
-                }
-                umma_commit(&bars.pv_done[t], leader);
-                if (j + 1 == w.n_kv[t]) umma_commit(&bars.o_full[t], leader);  // O_t of this item is complete
-              }
-              if (!ok) break;
-              umma_commit(&bars.kv_empty[s], leader);
+              if (ok) release_kv(j + 1, sn);
             }
+            ++g;  // the item's last key tile
           } else {
             for (int t = 0; ok && t < kTiles; ++t) {
               if (!warp_wait(&bars.q_full[t], it & 1, &bars.abort, &g_fwd_status)) {
@@ -457,6 +456,52 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         umma_commit(&bars.drain, leader);
         mbar_wait_drain(&bars.drain, 0);
       }
+      __syncwarp();
+    } else if (kSPrefetch && warp < kPvWarp0 + kTiles) {
+      // ------------------------------------------------------------ P V issuer of tile t
+      // Walks the same items and steps as the tile's softmax warps: O_t += P_t V(j)
+      // once the four warps have written P_t(j) (p_full).  Each mbarrier test costs a
+      // few hundred cycles while the tensor core streams operands from shared memory,
+      // and the tensor core's queue is shallow, so issuing eight MMAs can stall the
+      // issuing thread for several hundred more: with a warp of its own per tile,
+      // neither falls on the S products' issuer nor on the softmax.  The item's first
+      // product overwrites O_t; the softmax warps read O_t out in the previous item's
+      // epilogue, before they hand over that item's first P_t.
+      const int t = warp - kPvWarp0;
+      const uint32_t leader = elect_one() ? 1u : 0u;
+      const uint64_t dV = sdesc_sw128(smem_u32(sV), kBN * 128, 1024);  // V stage 0, MN-major
+      const uint32_t o_mma = tmem + C::kOCol + t * D, p_mma = tmem + C::kPCol + t * (kBN / 2);
+      constexpr uint32_t kIdO = idesc_bf16_f32(kBM, D, false, true);
+      int kv_pos = 0;  // K/V tiles of the items before this one (the ring position)
+      int step = 0;    // the tile's steps across items (the P barriers' phase)
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        const int ring = it % kItemRing;
+        if (!warp_wait(&bars.item_full[ring], (it / kItemRing) & 1, &bars.abort, &g_fwd_status)) break;
+        const int item = bars.item[ring];
+        const FwdItem w = bars.work[ring];
+        mbar_arrive_warp(&bars.item_empty[ring]);
+        if (item >= n_items) break;
+        const int n_kv_t = t == 0 ? w.n_kv[0] : w.n_kv[1];
+        for (int j = 0; j < n_kv_t; ++j, ++step) {
+          if (!warp_wait(&bars.p_full[t], step & 1, &bars.abort, &g_fwd_status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int stage = (kv_pos + j) % C::kStages;
+          const uint64_t v_d = desc_add(dV, stage * C::kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            umma_ts(o_mma, p_mma + kk * 8, desc_add(v_d, kk * 16 * 128), kIdO, (j > 0 || kk > 0) ? 1u : 0u, leader);
+          umma_commit(&bars.pv_done[t], leader);
+          umma_commit(&bars.kv_empty[stage], leader);
+        }
+        kv_pos += w.n_kv[kTiles - 1];
+      }
+      // Every P V product issued here completes before tensor memory is released.
+      umma_commit(&bars.drain_pv[t], leader);
+      if (lane == 0) mbar_wait_drain(&bars.drain_pv[t], 0);
       __syncwarp();
     }
   } else {
@@ -654,7 +699,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     // ------------------------------------------------------------ epilogue
     // The whole O row leaves tensor memory first; o_empty then lets the next item's
     // first P V product overwrite it while this row is normalised and stored.
-    if (!ok || !__all_sync(0xffffffffu, mbar_wait(&bars.o_full[t], it & 1, &bars.abort, &g_fwd_status))) {
+    // O_t is complete once the item's last P V product is; with S prefetch that is
+    // the tile's P V product before the step counter.  (The next item's first P V
+    // product overwrites O_t: with S prefetch its issuer waits for this warp's first
+    // P_t of that item, which comes after the loads below.)
+    if (!ok || !__all_sync(0xffffffffu, kSPrefetch ? mbar_wait(&bars.pv_done[t], (step - 1) & 1, &bars.abort, &g_fwd_status)
+                                                   : mbar_wait(&bars.o_full[t], it & 1, &bars.abort, &g_fwd_status))) {
       ok = false;
       break;
     }
@@ -666,7 +716,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       tmem_ld64(o_tm + c, part);
     }
     tc_fence_before();
-    mbar_arrive_warp(&bars.o_empty[t]);
+    if constexpr (!kSPrefetch) mbar_arrive_warp(&bars.o_empty[t]);
     {
       const float inv_l = 1.f / l_hat;
       const size_t row_off = (static_cast<size_t>(bh) * a.Nq + row) * D;
