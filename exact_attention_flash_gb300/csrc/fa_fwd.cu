@@ -11,8 +11,9 @@
 // last visible key are masked.
 //
 // GPU design (one CTA = two 128-row query tiles, 256 rows):
-//   warp 8      TMA producer: both Q tiles once, then K and V tiles of 128 keys
-//               through a ring of shared-memory stages.
+//   warp 8      TMA producer: claims work items (blocks of 256 query rows of one
+//               head), loads both Q tiles of each, then its K and V tiles of 128
+//               keys through a ring of shared-memory stages.
 //   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into TMEM (SS MMA),
 //               O_t += P_t V_j with P read from TMEM (TS MMA), interleaving the
 //               two tiles so the tensor core works on one tile while the other
