@@ -24,11 +24,11 @@
 //       dQ_i^T = K^T dS_i^T                      (SS MMA, M=d, N=64, dS from smem)
 //   warp 16 loads (TMA), warp 17 issues MMAs, warp 18 waits on the mbarriers the
 //   issuer depends on and hands each completion to it through a hardware named
-//   barrier, warps 0-7 (thread = key, two warpgroups by query half) turn S^T into
-//   P^T and then dP^T into dS^T, warps 8-15 (thread = feature) add dQ_i^T into dQ
-//   with fp32 reductions in L2.  S^T/dP^T are double-buffered in TMEM so the tensor
-//   core computes step n+1 while step n's elementwise work runs; dQ^T of step n
-//   lands in the dP^T buffer that dS^T of step n has just left.
+//   barrier, warps 0-7 (thread = key, two warpgroups taking alternate steps) turn
+//   S^T into P^T and then dP^T into dS^T, warps 8-15 (thread = feature) add dQ_i^T
+//   into dQ with fp32 reductions in L2.  S^T/dP^T are double-buffered in TMEM so the
+//   tensor core computes step n+1 while step n's elementwise work runs; dQ^T of step
+//   n lands in the dP^T buffer that dS^T of step n has just left.
 // Tensor memory (512 columns): S^T[2] [0,64) [64,128), dP^T[2] [128,192)
 // [192,256), dV [256, 256+d), dK [256+d, 256+2d).
 // Gradients leave as fp32, or as bf16: the epilogue rounds dK and dV, and dQ is
@@ -49,16 +49,18 @@ __device__ unsigned g_bwd_status;
 
 constexpr int kBKV = 128;  // keys per CTA
 constexpr int kBQ = 64;    // queries per step
-// Warps 0-7: P^T / dS^T and warps 8-15: dQ writers (each two warpgroups, one per
-// half of the step's 64 query columns); warp 16: TMA producer; warp 17: MMA
-// issuer; warp 18: the issuer's waits; warp 19 only lends its registers.
+// Warps 0-7: P^T / dS^T (two warpgroups, one per step parity) and warps 8-15: dQ
+// writers (two warpgroups, one per half of the step's 64 query columns); warp 16:
+// TMA producer; warp 17: MMA issuer; warp 18: the issuer's waits; warp 19 only
+// lends its registers.
 constexpr int kBwdThreads = 640;
 constexpr int kWriterWarp0 = 8;
 constexpr int kProducerWarp = 16;
 constexpr int kMmaWarp = 17;
 constexpr int kWaitWarp = 18;
-// Register split (setmaxnreg) by warpgroup: each P/dS thread holds two 32-column
-// TMEM rows, each dQ writer one 32-column row, the producer / MMA warps little.
+// Register split (setmaxnreg) by warpgroup: each P/dS thread holds a 64-query row of
+// P in fp32 and 32 columns of dP^T, each dQ writer one 32-column row, the producer /
+// MMA warps little.
 // The sum stays within the CTA's launch allocation; the launcher checks it.
 constexpr int kComputeRegs = 120;
 constexpr int kWriterRegs = 72;
@@ -188,8 +190,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.s_full[b], 1);
       mbar_init(&sh.dp_full[b], 1);
-      mbar_init(&sh.p_full[b], 8);   // one arrival per P/dS warp
-      mbar_init(&sh.ds_full[b], 8);
+      mbar_init(&sh.p_full[b], 4);   // one arrival per P/dS warp of the step's warpgroup
+      mbar_init(&sh.ds_full[b], 4);
       mbar_init(&sh.dq_full[b], 1);
       mbar_init(&sh.dq_empty[b], kDqWarpsPerStep<D>);  // one arrival per dQ writer warp of the step
       mbar_init(&sh.ds_empty[b], 1);
@@ -304,9 +306,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
                     desc_add(do_d, (kk >> 2) * (kBQ * 128) + (kk & 3) * 32), kIdSdP, 1u, leader);
           umma_commit(&sh.dp_full[n & 1], leader);
         };
-        // P^T of query half h sits packed in columns [32h, 32h + 16) of the S^T buffer,
-        // dS^T likewise in the dP^T buffer.
-        auto pcol = [](int kk) { return (kk >> 1) * 32 + (kk & 1) * 8; };
+        // P^T sits packed (queries 2c, 2c+1 in column c) in columns [0, 32) of the S^T
+        // buffer, dS^T likewise in the dP^T buffer: K = 16 queries per 8 columns.
+        auto pcol = [](int kk) { return kk * 8; };
         bool ok = issuer_rendezvous(true);  // K, V and Q(0) loaded
         if (ok) {
           tc_fence_after();
@@ -392,24 +394,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
   } else if (warp < kWriterWarp0) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kComputeRegs));
     // ------------------------------------------------------------ P^T and dS^T (thread = key)
-    // Warpgroup h takes query columns [32h, 32h + 32) of each step; each element is
-    // independent, so the two warpgroups never exchange data.
+    // Warpgroup h takes the steps n with n % 2 == h, whose S^T, dP^T and dS buffers
+    // are those of parity h, and forms P^T and then dS^T for all 64 queries of each.
+    // So two steps are in flight: one warpgroup's exponentials of step n + 1 run
+    // while the other still waits for dP^T(n) or forms dS^T(n), and P stays in
+    // registers in fp32 from the exponentials to dS.
     const int k = tid & (kBKV - 1);
     const int h = warp >> 2;
     const int key = key0 + k;
     const int lane_base = (warp & 3) * 32;
     const float sl2 = a.scale_log2;
     bool ok = true;
-    for (int n = 0; n < n_steps; ++n) {
+    for (int n = h; n < n_steps; n += 2) {
       const int b = n & 1;
       const int q0 = (i_start + n) * kBQ;
       // The dS tile of step n - 2 must have been read by dQ^T(n - 2) (checked first:
       // it is long done, and the check's latency hides behind the wait for S^T).
-      if (n >= 2 && !__all_sync(0xffffffffu, mbar_wait(&sh.ds_empty[b], ((n >> 1) - 1) & 1, &sh.abort, &g_bwd_status))) {
-        ok = false;
-        break;
-      }
-      if (!__all_sync(0xffffffffu, mbar_wait(&sh.s_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status))) {
+      if ((n >= 2 &&
+           !__all_sync(0xffffffffu, mbar_wait(&sh.ds_empty[b], ((n >> 1) - 1) & 1, &sh.abort, &g_bwd_status))) ||
+          !__all_sync(0xffffffffu, mbar_wait(&sh.s_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status))) {
         ok = false;
         break;
       }
@@ -417,36 +420,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       const bool need_mask = (a.causal && key0 + kBKV - 1 > a.q_start + q0) || (key0 + kBKV > a.Nk);
       const int first_visible_q = a.causal ? key - a.q_start : 0;  // queries before this one see nothing of the key
       const bool key_valid = key < a.Nk;
-      const uint32_t s_tm = tmem_addr(tmem, lane_base, b * kBQ + 32 * h);
-      const uint32_t dp_tm = tmem_addr(tmem, lane_base, 128 + b * kBQ + 32 * h);
-      // P^T first, while the tensor core still computes dP^T.  S^T arrives holding
-      // S^T - LSE/scale (the bias came with the product).
-      uint32_t sv[32];
-      tmem_ld32(s_tm, sv);
-      // The exponentials are issued back to back (all arguments first, then all 32
-      // ex2, then the packs), so that the special-function unit's latency overlaps
-      // across them instead of each result being waited for by its pack.
-      float p[32];
-      uint32_t pk[16];
-      const float2 sl2x2 = make_float2(sl2, sl2);
+      const uint32_t s_tm = tmem_addr(tmem, lane_base, b * kBQ);
+      const uint32_t dp_tm = tmem_addr(tmem, lane_base, 128 + b * kBQ);
+      // S^T arrives holding S^T - LSE/scale (the bias came with the product).  The
+      // exponentials are issued back to back (all arguments first, then all 64 ex2,
+      // then the packs), so that the special-function unit's latency overlaps across
+      // them instead of each result being waited for by its pack.
+      float p[64];
+      {
+        uint32_t sv[64];
+        tmem_ld64(s_tm, sv);
+        const float2 sl2x2 = make_float2(sl2, sl2);
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const float2 arg = __fmul2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2x2);
-        p[e] = arg.x;
-        p[e + 1] = arg.y;
+        for (int e = 0; e < 64; e += 2) {
+          const float2 arg = __fmul2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2x2);
+          p[e] = arg.x;
+          p[e + 1] = arg.y;
+        }
       }
 #pragma unroll
-      for (int e = 0; e < 32; ++e) p[e] = ex2(p[e]);
+      for (int e = 0; e < 64; ++e) p[e] = ex2(p[e]);
       if (need_mask) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (!key_valid || q0 + 32 * h + e < first_visible_q) p[e] = 0.f;
+        for (int e = 0; e < 64; ++e)
+          if (!key_valid || q0 + e < first_visible_q) p[e] = 0.f;
       }
+      {
+        // P^T packed (queries 2c, 2c+1 in column c) over columns [0, 32) of the
+        // buffer, which this thread has already read.
+        uint32_t pk[32];
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) pk[e / 2] = pack_bf16(p[e], p[e + 1]);
-      // P^T packed (queries 2c, 2c+1 in column c) over the first 16 of this half's 32
-      // columns, which this thread has already read.
-      tmem_st16(s_tm, pk);
+        for (int e = 0; e < 64; e += 2) pk[e / 2] = pack_bf16(p[e], p[e + 1]);
+        tmem_st32(s_tm, pk);
+      }
       tc_fence_before();
       mbar_arrive_warp(&sh.p_full[b]);
       if (!__all_sync(0xffffffffu, mbar_wait(&sh.dp_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status))) {
@@ -457,25 +463,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       // dS^T = P^T * (dP^T - D); dP^T arrives holding dP^T - D.  The softmax scale of
       // dQ = dS K * scale and dK = dS^T Q * scale is applied here, once per element of
       // dS (rounding scale * dS to bf16 has the relative error of rounding dS), so the
-      // dQ writers and the dK epilogue add and store the products as they are.
-      uint32_t dpv[32];
-      tmem_ld32(dp_tm, dpv);
-      uint32_t dk[16];
+      // dQ writers and the dK epilogue add and store the products as they are.  dP^T
+      // is read 32 columns at a time, which keeps the fp32 P and dP^T within the
+      // registers of this role.
+      uint32_t dk[32];
       const float2 sc2 = make_float2(a.scale, a.scale);
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const float2 ds2 = __fmul2_rn(__fmul2_rn(make_float2(p[e], p[e + 1]), sc2),
-                                      make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])));
-        dk[e / 2] = pack_bf16(ds2.x, ds2.y);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t dpv[32];
+        tmem_ld32(dp_tm + 32 * half, dpv);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float2 ds2 = __fmul2_rn(__fmul2_rn(make_float2(p[32 * half + e], p[32 * half + e + 1]), sc2),
+                                        make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])));
+          dk[16 * half + e / 2] = pack_bf16(ds2.x, ds2.y);
+        }
       }
       // dS^T row of this key into the MN-major, 128B-swizzled dS tile:
-      // 16-byte piece p (queries 8p..8p+7) of row k sits at ((p ^ (k & 7)) * 16).
+      // 16-byte piece j (queries 8j..8j+7) of row k sits at ((j ^ (k & 7)) * 16).
       uint8_t* ds_row = sDS + b * C::kDSBytes + (k >> 3) * 1024 + (k & 7) * 128;
 #pragma unroll
-      for (int piece = 0; piece < 4; ++piece)
-        *reinterpret_cast<uint4*>(ds_row + (((4 * h + piece) ^ (k & 7)) << 4)) =
+      for (int piece = 0; piece < 8; ++piece)
+        *reinterpret_cast<uint4*>(ds_row + ((piece ^ (k & 7)) << 4)) =
             make_uint4(dk[4 * piece], dk[4 * piece + 1], dk[4 * piece + 2], dk[4 * piece + 3]);
-      tmem_st16(dp_tm, dk);
+      tmem_st32(dp_tm, dk);
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive_warp(&sh.ds_full[b]);
