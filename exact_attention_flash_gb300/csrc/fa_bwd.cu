@@ -70,6 +70,12 @@ constexpr int kRegsNeeded = 256 * kComputeRegs + 256 * kWriterRegs + 128 * kOthe
 // whose lane quarters hold that step's features (see the dQ writers).
 template <int D>
 constexpr int kDqWarpsPerStep = D == 64 ? 4 : 8;
+// Where the P/dS warps wait for the dS tile of step n - 2 to have been read: at
+// d = 128 just before they write step n's tile, so that the exponentials of step n
+// never wait for dQ^T(n - 2), which the writers' pace holds back; at d = 64 at the
+// top of the step, where the wait's own latency hides behind the wait for S^T.
+template <int D>
+constexpr bool kLateDsWait = D == 128;
 
 template <int D>
 struct BwdCfg {
@@ -408,9 +414,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     for (int n = h; n < n_steps; n += 2) {
       const int b = n & 1;
       const int q0 = (i_start + n) * kBQ;
-      // The dS tile of step n - 2 must have been read by dQ^T(n - 2) (checked first:
-      // it is long done, and the check's latency hides behind the wait for S^T).
-      if ((n >= 2 &&
+      // The dS tile of step n - 2 must have been read by dQ^T(n - 2) (see kLateDsWait).
+      if ((!kLateDsWait<D> && n >= 2 &&
            !__all_sync(0xffffffffu, mbar_wait(&sh.ds_empty[b], ((n >> 1) - 1) & 1, &sh.abort, &g_bwd_status))) ||
           !__all_sync(0xffffffffu, mbar_wait(&sh.s_full[b], (n >> 1) & 1, &sh.abort, &g_bwd_status))) {
         ok = false;
@@ -478,6 +483,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
                                         make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])));
           dk[16 * half + e / 2] = pack_bf16(ds2.x, ds2.y);
         }
+      }
+      if (kLateDsWait<D> && n >= 2 &&
+          !__all_sync(0xffffffffu, mbar_wait(&sh.ds_empty[b], ((n >> 1) - 1) & 1, &sh.abort, &g_bwd_status))) {
+        ok = false;
+        break;
       }
       // dS^T row of this key into the MN-major, 128B-swizzled dS tile:
       // 16-byte piece j (queries 8j..8j+7) of row k sits at ((j ^ (k & 7)) * 16).
