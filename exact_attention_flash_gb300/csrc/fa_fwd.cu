@@ -57,13 +57,18 @@ constexpr int kSoftmaxRegs = 216;
 constexpr int kOtherRegs = 72;
 constexpr int kRegsNeeded = 256 * kSoftmaxRegs + 128 * kOtherRegs;
 // Lazy rescaling: the reference max m of a row moves (and O is rescaled) only when
-// a tile's max exceeds it by more than this many log2 units, so the weights
+// a tile's max exceeds it by more than kRescaleThreshold log2 units, so the weights
 // 2^(s - m) stay below 2^32.  fp32 and bf16 share one exponent range: the sum of N
 // weights stays below 2^(32 + log2 N) and O below that times max|v|, inside fp32
-// for N < 2^31 and |v| < 2^64.  Rounding of P to bf16 is relative, so the
-// threshold does not change the error of O; it only makes rescales rare when the
-// row max keeps rising (large logits).
+// for N < 2^31 and |v| < 2^64.  When it moves, the reference is set kRescaleHeadroom
+// units above the tile's max, so the row max may rise by threshold + headroom = 96
+// units before the next rescale; the row's largest weight is then at least 2^-64,
+// and weights that flush to zero (below 2^-126) are below 2^-62 of it, far under
+// fp32's 2^-24.  Rounding of P to bf16 is relative, so neither constant changes the
+// error of O; they only make rescales rare when the row max keeps rising (large
+// logits), where the warp-wide rescale of O otherwise runs on most steps.
 constexpr float kRescaleThreshold = 32.0f;
+constexpr float kRescaleHeadroom = 64.0f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D>
@@ -584,7 +589,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       float m_use = m_run;
       float alpha = 1.f;
       if (m_tile > m_run + kRescaleThreshold) {
-        m_use = m_tile;
+        m_use = m_tile + kRescaleHeadroom;
         alpha = ex2(m_run - m_use);  // 0 on the first tile
       }
       // Rescale this row of O when the reference max moved (not on the first
@@ -592,13 +597,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       // this waits for the previous P V product (below, before P_t is written).
       const auto rescale_o = [&]() {
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // 32 columns at a time (a wider load spills next to the row of S held in
+          // registers); the stores are waited for once, at the end.
+#pragma unroll
           for (int c = 0; c < D; c += 32) {
             uint32_t u[32];
             tmem_ld32(o_tm + c, u);
 #pragma unroll
             for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-            tmem_st32(o_tm + c, u);
+            tmem_st32_nowait(o_tm + c, u);
           }
+          tmem_wait_st();
         }
       };
       if constexpr (!kSPrefetch) rescale_o();
