@@ -76,6 +76,13 @@ constexpr int kDqWarpsPerStep = D == 64 ? 4 : 8;
 // top of the step, where the wait's own latency hides behind the wait for S^T.
 template <int D>
 constexpr bool kLateDsWait = D == 128;
+// d = 64: dS^T is stored over columns [32, 64) of the S^T buffer (free once P^T sits
+// packed in [0, 32) and S^T is in registers), which leaves the whole dP^T buffer free
+// as soon as the P/dS warps have read dP^T, so dQ^T(n) is issued before dK(n) and the
+// writers start earlier.  At d = 128, where the writers pace the step, issuing dQ^T
+// first was slower (it delays dK(n) and the release of the step's Q/dO stage).
+template <int D>
+constexpr bool kDqBeforeDk = D == 64;
 
 template <int D>
 struct BwdCfg {
@@ -282,8 +289,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
         const uint64_t dOnes = sdesc_k16_noswizzle(smem_u32(sOnes));        // A of the bias products
         const uint64_t dBias = sdesc_k16_noswizzle(smem_u32(sBias));        // bias tiles, stage 0
         // Per step n the products go in the order S^T(n+1), dV(n), dP^T(n+1), dK(n),
-        // dQ^T(n), each after a rendezvous with the waiting warp (warp 18) that covers
-        // what it reads or overwrites:
+        // dQ^T(n) (d = 64: dQ^T(n) before dK(n)), each after a rendezvous with the
+        // waiting warp (warp 18) that covers what it reads or overwrites:
         //   S^T(n+1)  Q(n+1) loaded; its buffer's previous user, dV(n-1), came earlier;
         //   dV(n)     P^T(n) in TMEM;
         //   dP^T(n+1) the dQ writers have read dQ^T(n-1) from the same buffer;
@@ -345,24 +352,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
           }
           if (!(ok = issuer_rendezvous(true))) break;
           tc_fence_after();
-          // dK += dS^T Q_i
-          const uint64_t q_d = desc_add(dQ_mn, s * C::kQBytes);
+          // dK += dS^T Q_i (dS^T packed in the dP^T buffer, or in the S^T buffer's upper
+          // half when dQ^T goes first; see kDqBeforeDk).
+          auto issue_dk = [&]() {
+            const uint64_t q_d = desc_add(dQ_mn, s * C::kQBytes);
+            const uint32_t ds_tm = kDqBeforeDk<D> ? s_tm + 32 : s_tm + 128;
   #pragma unroll
-          for (int kk = 0; kk < kBQ / 16; ++kk)
-            umma_ts(tmem + C::kDKCol, s_tm + 128 + pcol(kk), desc_add(q_d, kk * 16 * 128), kIdKV, kk > 0 ? 1u : acc0, leader);
-          umma_commit(&sh.q_empty[s], leader);
-          // dQ_i^T = K^T dS^T into the dP^T buffer (its dS^T was consumed by the dK MMA above).
+            for (int kk = 0; kk < kBQ / 16; ++kk)
+              umma_ts(tmem + C::kDKCol, ds_tm + pcol(kk), desc_add(q_d, kk * 16 * 128), kIdKV, kk > 0 ? 1u : acc0, leader);
+            umma_commit(&sh.q_empty[s], leader);
+          };
+          // dQ_i^T = K^T dS^T into the dP^T buffer, once nothing reads dS^T or dP^T there.
           // A = K as an MN-major [d x keys] operand.  For d = 64 only 64 of the M = 128
           // rows are features: even steps put them in lanes 0..63 (the other rows read
           // whatever follows K), odd steps in lanes 64..127 (the other rows read V), so
           // that the two halves of the dQ writers take alternate steps.
-          const uint64_t ds_d = desc_add(dDS_mn, b * C::kDSBytes);
-          const uint64_t dq_a = (D == 64 && (n & 1)) ? dK_mn_hi : dK_mn;
+          auto issue_dq = [&]() {
+            const uint64_t ds_d = desc_add(dDS_mn, b * C::kDSBytes);
+            const uint64_t dq_a = (D == 64 && (n & 1)) ? dK_mn_hi : dK_mn;
   #pragma unroll
-          for (int kk = 0; kk < kBKV / 16; ++kk)
-            umma_ss(s_tm + 128, desc_add(dq_a, kk * 16 * 128), desc_add(ds_d, kk * 16 * 128), kIdQ, kk > 0, leader);
-          umma_commit(&sh.dq_full[b], leader);
-          umma_commit(&sh.ds_empty[b], leader);
+            for (int kk = 0; kk < kBKV / 16; ++kk)
+              umma_ss(s_tm + 128, desc_add(dq_a, kk * 16 * 128), desc_add(ds_d, kk * 16 * 128), kIdQ, kk > 0, leader);
+            umma_commit(&sh.dq_full[b], leader);
+            umma_commit(&sh.ds_empty[b], leader);
+          };
+          if constexpr (kDqBeforeDk<D>) {
+            issue_dq();
+            issue_dk();
+          } else {
+            issue_dk();
+            issue_dq();
+          }
         }
         if (ok) umma_commit(&sh.dkdv_full, leader);
         umma_commit(&sh.drain, leader);
@@ -496,7 +516,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       for (int piece = 0; piece < 8; ++piece)
         *reinterpret_cast<uint4*>(ds_row + ((piece ^ (k & 7)) << 4)) =
             make_uint4(dk[4 * piece], dk[4 * piece + 1], dk[4 * piece + 2], dk[4 * piece + 3]);
-      tmem_st32(dp_tm, dk);
+      tmem_st32(kDqBeforeDk<D> ? s_tm + 32 : dp_tm, dk);
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive_warp(&sh.ds_full[b]);
