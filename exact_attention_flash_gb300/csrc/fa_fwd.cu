@@ -64,11 +64,16 @@ constexpr int kRegsNeeded = 256 * kSoftmaxRegs + 128 * kOtherRegs;
 // units above the tile's max, so the row max may rise by threshold + headroom = 96
 // units before the next rescale; the row's largest weight is then at least 2^-64,
 // and weights that flush to zero (below 2^-126) are below 2^-62 of it, far under
-// fp32's 2^-24.  Rounding of P to bf16 is relative, so neither constant changes the
-// error of O; they only make rescales rare when the row max keeps rising (large
-// logits), where the warp-wide rescale of O otherwise runs on most steps.
+// fp32's 2^-24.  The rescale factor 2^(m_old - m_new) flushes to zero when the max
+// jumps by more than 126 - headroom units; the old terms it drops are then below
+// 2^(threshold + headroom - 126) of the new largest weight, so threshold + headroom
+// must stay at or below 102 (a headroom of 96 dropped terms as large as the new ones).
+// Rounding of P to bf16 is relative, so neither constant changes the error of O;
+// they only make rescales rare when the row max keeps rising (large logits), where
+// the warp-wide rescale of O otherwise runs on most steps.
 constexpr float kRescaleThreshold = 32.0f;
 constexpr float kRescaleHeadroom = 64.0f;
+static_assert(kRescaleThreshold + kRescaleHeadroom <= 102.0f, "a flushed rescale factor must drop only terms below 2^-24");
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D>
