@@ -28,7 +28,8 @@
 //   S^T into P^T and then dP^T into dS^T, warps 8-15 (thread = feature) add dQ_i^T
 //   into dQ with fp32 reductions in L2.  S^T/dP^T are double-buffered in TMEM so the
 //   tensor core computes step n+1 while step n's elementwise work runs; dQ^T of step
-//   n lands in the dP^T buffer that dS^T of step n has just left.
+//   n lands in the dP^T buffer (d = 128: after dK(n) has read dS^T(n) from it; d = 64:
+//   dS^T(n) sits in the upper half of the S^T buffer, so dQ^T(n) goes before dK(n)).
 // Tensor memory (512 columns): S^T[2] [0,64) [64,128), dP^T[2] [128,192)
 // [192,256), dV [256, 256+d), dK [256+d, 256+2d).
 // Gradients leave as fp32, or as bf16: the epilogue rounds dK and dV, and dQ is
