@@ -11,9 +11,11 @@
 // identity); two empty runs give O = 0 and LSE = -inf, as the page's guarded base
 // (0 when both maxima are -inf) does.
 //
-// One warp per row, grid-stride over the rows; each lane moves 4 consecutive
-// elements per access (16 bytes of fp32 or 8 of bf16), so a warp covers 128
-// elements per instruction.  HBM-bound: 3 row reads / writes of O per row.
+// d = 64 and 128 (merge_kernel_t): every lane moves 16 bytes per access (4 fp32 or
+// 8 bf16 elements), so a warp holds 1 to 4 whole rows, and each warp keeps two passes
+// of rows in flight with all their loads issued before any result is used.  Other d
+// (merge_kernel): one warp per row, 4 elements per lane and access.  Grid-stride over
+// the rows; HBM-bound: 3 row reads / writes of O per row.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -86,6 +88,72 @@ __global__ void __launch_bounds__(256) merge_kernel(const void* __restrict__ o_a
   }
 }
 
+// d = 64 or 128: each lane moves 16 bytes per access (4 fp32 or 8 bf16 elements), so
+// a row takes d / 4 or d / 8 lanes and a warp holds 1 to 4 rows; each warp keeps two
+// passes of rows in flight, every load of both issued before any result is used.
+template <int D, bool F32>
+__global__ void __launch_bounds__(256) merge_kernel_t(const void* __restrict__ o_a, const float* __restrict__ lse_a,
+                                                      const void* __restrict__ o_b, const float* __restrict__ lse_b,
+                                                      void* o, float* lse, long long rows) {
+  constexpr int kPerLane = F32 ? 4 : 8;
+  constexpr int kLanesPerRow = D / kPerLane;
+  constexpr int kRowsPerPass = 32 / kLanesPerRow;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / kLanesPerRow, col = kPerLane * (lane % kLanesPerRow);
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  const long long gwarp = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  for (long long slot = gwarp; slot * kRowsPerPass < rows; slot += 2 * warps) {
+    long long row[2];
+    bool ok[2];
+    float la[2], lb[2];
+    uint4 ra[2], rb[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      row[u] = (slot + u * warps) * kRowsPerPass + sub;
+      ok[u] = row[u] < rows && in_bounds(row[u] * D + col + kPerLane - 1, rows * D, &g_merge_status);
+      if (ok[u]) {
+        la[u] = lse_a[row[u]];
+        lb[u] = lse_b[row[u]];
+        const size_t off = static_cast<size_t>(row[u] * D + col) * (F32 ? 4 : 2);
+        ra[u] = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(o_a) + off);
+        rb[u] = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(o_b) + off);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (!ok[u]) continue;
+      const float m = fmaxf(la[u], lb[u]);
+      float wa = 0.f, wb = 0.f;
+      if (m != -INFINITY) {  // both empty: O = 0, LSE = -inf
+        wa = expf(la[u] - m);
+        wb = expf(lb[u] - m);
+      }
+      const float s = wa + wb;
+      const float inv = s > 0.f ? 1.f / s : 0.f;
+      const float ca = wa * inv, cb = wb * inv;
+      const uint32_t a4[4] = {ra[u].x, ra[u].y, ra[u].z, ra[u].w}, b4[4] = {rb[u].x, rb[u].y, rb[u].z, rb[u].w};
+      uint32_t r4[4];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        if (F32) {
+          r4[w] = __float_as_uint(ca * __uint_as_float(a4[w]) + cb * __uint_as_float(b4[w]));
+        } else {
+          const float lo = ca * __uint_as_float(a4[w] << 16) + cb * __uint_as_float(b4[w] << 16);
+          const float hi = ca * __uint_as_float(a4[w] & 0xFFFF0000u) + cb * __uint_as_float(b4[w] & 0xFFFF0000u);
+          r4[w] = pack_bf16(lo, hi);
+        }
+      }
+      const size_t off = static_cast<size_t>(row[u] * D + col) * (F32 ? 4 : 2);
+      *reinterpret_cast<uint4*>(static_cast<uint8_t*>(o) + off) = make_uint4(r4[0], r4[1], r4[2], r4[3]);
+      la[u] = m == -INFINITY ? -INFINITY : m + logf(s);
+    }
+    __syncwarp();  // every lane has read its rows' LSE inputs before they may be overwritten in place
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      if (ok[u] && col == 0) lse[row[u]] = la[u];
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o, float* lse,
@@ -95,8 +163,18 @@ cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b, c
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const long long blocks_needed = (rows + 7) / 8;  // 8 warps (rows at a time) per block
   const long long cap = static_cast<long long>(sms) * 16;
+  if (d == 64 || d == 128) {
+    const long long per_block = 8LL * 2 * (32 / (d / (o_f32 ? 4 : 8)));  // 8 warps, two passes of rows
+    const long long blocks_needed = (rows + per_block - 1) / per_block;
+    const unsigned grid = static_cast<unsigned>(blocks_needed < cap ? blocks_needed : cap);
+    if (d == 64 && o_f32) merge_kernel_t<64, true><<<grid, 256, 0, stream>>>(o_a, lse_a, o_b, lse_b, o, lse, rows);
+    if (d == 64 && !o_f32) merge_kernel_t<64, false><<<grid, 256, 0, stream>>>(o_a, lse_a, o_b, lse_b, o, lse, rows);
+    if (d == 128 && o_f32) merge_kernel_t<128, true><<<grid, 256, 0, stream>>>(o_a, lse_a, o_b, lse_b, o, lse, rows);
+    if (d == 128 && !o_f32) merge_kernel_t<128, false><<<grid, 256, 0, stream>>>(o_a, lse_a, o_b, lse_b, o, lse, rows);
+    return cudaGetLastError();
+  }
+  const long long blocks_needed = (rows + 7) / 8;  // 8 warps (rows at a time) per block
   const unsigned grid = static_cast<unsigned>(blocks_needed < cap ? blocks_needed : cap);
   merge_kernel<<<grid, 256, 0, stream>>>(o_a, lse_a, o_b, lse_b, o, lse, rows, d, o_f32);
   return cudaGetLastError();
