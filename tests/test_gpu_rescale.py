@@ -41,7 +41,8 @@ def _gpu():
     require_gpu()
 
 
-def _inputs(kind, d, rows=256, seed=7):
+def inputs_cpu(kind, d, rows=256, seed=7):
+    """q [1, 1, rows, d], k and v [1, 1, 128 * tiles, d], bf16 on the CPU."""
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)
     ladder = LADDERS[(kind, d)]
@@ -51,7 +52,11 @@ def _inputs(kind, d, rows=256, seed=7):
     k = torch.randn(1, 1, n, d, generator=g)
     k[..., 0] = torch.tensor(ladder).repeat_interleave(128)
     v = torch.randn(1, 1, n, d, generator=g) + torch.tensor(V_OFFSET).repeat_interleave(128)[None, None, :, None]
-    return tuple(t.to(torch.bfloat16).cuda() for t in (q, k, v))
+    return tuple(t.to(torch.bfloat16) for t in (q, k, v))
+
+
+def _inputs(kind, d):
+    return tuple(t.cuda() for t in inputs_cpu(kind, d))
 
 
 @pytest.mark.parametrize("d", [64, 128])
